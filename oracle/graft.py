@@ -1,0 +1,97 @@
+"""Graft's successor table: online update, stage templates, retrieval.
+
+Graft page section 2 (second gear): a V x k integer table lives in GPU
+memory; row t holds the k most probable tokens to follow token t.  Retrieval
+expands a subtree rooted at the current token by following a fixed
+stage-adaptive template over the table; the template is asymmetric — the
+top-ranked successor gets more children and a deeper greedy chain, lower
+ranks fewer.  The verification budget is 60 slots, split between kept draft
+nodes and retrieved nodes as 8/52 (pruned at the root), 24/36 (depth 1),
+40/20 (depth 5) and 60/0 (not pruned).  Section 5: the best retrieval depth
+and width are both about 8.  Section 2 (third gear) and section 6: after
+verification every verified position — accepted or rejected — rewrites the
+row of its token with the target's top-k next tokens.
+
+Readings used here:
+  * conflicts: when several verified nodes carry the same token, the last in
+    (request, node) order wins; the row is overwritten, not merged;
+  * template: best-first over rank paths (r_1..r_d), d <= 8, r < k, with
+    weight prod_j w(r_j), w(r) = 0.9 * 0.4**r; equal weights are broken by
+    the lexicographically smaller path; the first S paths form the template.
+    Every path's weight is below its prefix's, so the template is
+    prefix-closed and parents precede children.  The pages fix only the
+    qualitative shape, so the exact slots are *parity unpinned* against the
+    pages (the retrieval given a template is pinned).
+  * the retrieved subtree hangs off the tree root (the current token).
+"""
+from __future__ import annotations
+
+import heapq
+from fractions import Fraction
+
+import numpy as np
+
+STAGE_SLOTS = (52, 36, 20, 0)   # retrieval slots for stages root, depth1, depth5, none
+
+
+def adj_update(adj, tok, topk_idx, valid=None):
+    """In place: for each valid node in order, adj[tok[i], :] = topk_idx[i, :k]."""
+    k = adj.shape[1]
+    for i in range(len(tok)):
+        if valid is not None and not valid[i]:
+            continue
+        adj[int(tok[i]), :] = topk_idx[i, :k]
+    return adj
+
+
+def stage_template(S, k=8, max_depth=8, w0=Fraction(9, 10), decay=Fraction(2, 5)):
+    """First S rank paths in best-first order; returns (tparent, trank) int32 [S].
+
+    tparent[s] is the slot index of the path's prefix (-1 = the root token),
+    trank[s] the last rank of the path.  Exact rational weights."""
+    w = [w0 * decay ** r for r in range(k)]
+    heap = [(-w[r], (r,)) for r in range(k)]
+    heapq.heapify(heap)
+    slot_of = {}
+    tparent, trank = [], []
+    while heap and len(tparent) < S:
+        negw, path = heapq.heappop(heap)
+        slot_of[path] = len(tparent)
+        tparent.append(slot_of[path[:-1]] if len(path) > 1 else -1)
+        trank.append(path[-1])
+        if len(path) < max_depth:
+            for r in range(k):
+                heapq.heappush(heap, (negw * w[r], path + (r,)))
+    return np.array(tparent, np.int32), np.array(trank, np.int32)
+
+
+def stage_templates(k=8, max_depth=8, slots=STAGE_SLOTS):
+    """Concatenated per-stage templates plus offsets [n_stage + 1]."""
+    tp, tr, off = [], [], [0]
+    for S in slots:
+        p, r = stage_template(S, k, max_depth)
+        tp.append(p)
+        tr.append(r)
+        off.append(off[-1] + S)
+    return (np.concatenate(tp).astype(np.int32), np.concatenate(tr).astype(np.int32),
+            np.array(off, np.int32))
+
+
+def retrieve(adj, root_tok, stage, tparent, trank, tmpl_off, max_slots):
+    """Template expansion per request.  Slot s of request b:
+    tok = adj[tok_of(tparent[s]), trank[s]], tok_of(-1) = root_tok[b].
+    Returns rtok [B, max_slots], rparent [B, max_slots] (-1 padded) and nslots [B]."""
+    B = len(root_tok)
+    rtok = np.full((B, max_slots), -1, np.int32)
+    rpar = np.full((B, max_slots), -1, np.int32)
+    nslots = np.zeros(B, np.int32)
+    for b in range(B):
+        st = int(stage[b])
+        s0, s1 = int(tmpl_off[st]), int(tmpl_off[st + 1])
+        for s in range(s1 - s0):
+            p = int(tparent[s0 + s])
+            src = int(root_tok[b]) if p < 0 else int(rtok[b, p])
+            rtok[b, s] = adj[src, int(trank[s0 + s])]
+            rpar[b, s] = p
+        nslots[b] = s1 - s0
+    return rtok, rpar, nslots
