@@ -1,0 +1,539 @@
+"""Benchmark: batched speculative-tree verification on GB300 (libtreeverify).
+
+Headline workload: D-cut batched block verify at batch 64 — each request a
+chain of 1 bonus + 15 draft tokens over a prefix of 512..4096 tokens,
+Qwen3-8B attention geometry (32 q heads, 8 KV heads, head_dim 128, bf16),
+Qwen3 vocabulary (151936) bf16 logits.  One step = the whole verification
+path for the batch:
+  dcut_select -> tv_tree_prep -> tree_verify_attn (kept prefix of each chain)
+  -> vocab_argmax_topk (kept rows, k = 8) -> accept_longest_path
+  -> graft_adj_update (every verified node's top-8) -> graft_retrieve
+     (next step's retrieval candidates from each request's bonus token)
+Metric: verified tree nodes per second (kept positions per step / step time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--rho 0.5] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the same workload (a bounded sample of requests per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "verified tree nodes/s per GB300 at bs=64; HBM GB/s & TC util vs chip peak"
+UNIT = "nodes/s"
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD = "dcut_batch_bs64"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--rho", type=float, default=0.5, help="D-cut budget ratio verified per step")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row kernel measurements")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def config_dict(rho, n_gpus):
+    return {"workload": WORKLOAD, "batch": 64, "draft_len": 15, "nodes_per_request": 16,
+            "prefix_len": "uniform 512..4096", "attention": "32q/8kv heads, d=128, bf16",
+            "vocab": synth.QWEN3_VOCAB, "topk": 8, "rho": rho, "rhos_selected": list(synth.DCUT_RHOS),
+            "graft_table": "151936x8 int32", "retrieval_stage": "depth5 (20 slots)",
+            "l2": "inputs exceed L2 (>700 MB read per step vs 129 MB L2); no flush needed",
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
+
+
+# ============================================================ CPU oracle arm
+def _oracle_request(args):
+    """Oracle verification of one request of the batch (run in a worker)."""
+    (r, N, sel, keep_row, parent, tok, logits_rows, q, kt, vt, kp, vp) = args
+    from oracle import accept as oacc, attention as oatt, vocab as ovoc
+    cnt = int(keep_row.sum())
+    off = np.array([0, N], np.int32)
+    oatt.tree_attention(q, kp, vp, np.array([0, kp.shape[0]], np.int32), kt, vt, off, parent,
+                        node_cnt=np.array([cnt]))
+    am, ti, _, _, _ = ovoc.argmax_topk(logits_rows, 8)
+    argmax = np.full(N, -1, np.int32)
+    argmax[:cnt] = am
+    oacc.accept_longest_path(parent, tok, argmax, off, keep_row)
+    return cnt, ti
+
+
+def oracle_step(d, requests, pool, rho, adj, tmpl):
+    """One oracle step on a sample of requests.  Returns verified nodes."""
+    from oracle import dcut as odc, graft as ogr
+    B, N = d["B"], d["D"] + 1
+    s, keep, keep_len, pack_off, pack_idx = odc.select(d["conf"], [rho])
+    jobs = []
+    for r in requests:
+        cnt = int(keep_len[0, r])
+        p0, p1 = int(d["pre_off"][r]), int(d["pre_off"][r + 1])
+        sl = slice(r * N, (r + 1) * N)
+        jobs.append((r, N, None, keep[0, r], d["parent"][sl], d["tok"][sl],
+                     d["logits"][r * N:r * N + cnt], d["q"][sl], d["k_tree"][sl], d["v_tree"][sl],
+                     d["k_pre"][p0:p1], d["v_pre"][p0:p1]))
+    res = pool.map(_oracle_request, jobs) if pool else [_oracle_request(j) for j in jobs]
+    nodes = 0
+    for (r, *_), (cnt, ti) in zip(jobs, res):
+        nodes += cnt
+        ogr.adj_update(adj, d["tok"][r * N:r * N + cnt], ti)
+    tp, tr, off = tmpl
+    ogr.retrieve(adj, d["tok"][[r * N for r in requests]], np.full(len(requests), 2), tp, tr, off, 52)
+    return nodes
+
+
+def run_cpu_oracle(d, rho, steps, warmup, budget_s):
+    """Time the oracle on bounded samples.  Returns (nodes/s, cores, sample text, sec/step)."""
+    from oracle import graft as ogr
+    tmpl = ogr.stage_templates()
+    adj = synth.successor_table(3)
+    cores = max(1, min(os.cpu_count() or 1, 16))
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(cores)
+    try:
+        t0 = time.perf_counter()
+        oracle_step(d, list(range(cores)), pool, rho, adj, tmpl)     # pool start-up + calibration
+        t_one = (time.perf_counter() - t0) / cores
+        per_step = max(budget_s / max(1, steps + warmup), t_one)
+        n_req = int(min(d["B"], max(1, round(per_step / t_one * cores / 2))))
+        reqs = [(7 * i) % d["B"] for i in range(n_req)]
+        for _ in range(warmup):
+            oracle_step(d, reqs, pool, rho, adj, tmpl)
+        nodes, t = 0, 0.0
+        for _ in range(steps):
+            a = time.perf_counter()
+            nodes += oracle_step(d, reqs, pool, rho, adj, tmpl)
+            t += time.perf_counter() - a
+    finally:
+        pool.close()
+        pool.join()
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    sample = (f"{n_req} of 64 requests per step (selection over the whole batch), fp64 NumPy oracle, "
+              f"{cores} single-threaded worker processes")
+    return nodes / t, cores, sample, t / steps
+
+
+# ============================================================ GPU arm
+def to_dev(a, torch, pin=False):
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+    if pin:
+        return t.pin_memory()
+    return t.cuda()
+
+
+def make_step(tv, torch, hd, rho):
+    """hd: dict of device tensors.  All outputs and workspaces are allocated
+    here, once, so the step itself launches only libtreeverify kernels.
+    Returns (step_fn, kernels, out, K)."""
+    B, D = hd["B"], hd["D"]
+    N = D + 1
+    V = synth.QWEN3_VOCAB
+    rhos = list(synth.DCUT_RHOS)
+    if rho not in rhos:
+        rhos.append(rho)
+    ri = rhos.index(rho)
+    total = B * N
+    K = int(math.floor(float(np.float32(rho)) * total + 0.5))
+    tp, tr, toff = tv.stage_templates()
+    tmpl = [to_dev(x, torch) for x in (tp, tr, toff)]
+    stage = torch.full((B,), 2, dtype=torch.int32, device="cuda")
+    max_prefix = int(hd["max_prefix"])
+    lib = tv.load_library()
+    e32 = lambda *s: torch.empty(s, dtype=torch.int32, device="cuda")
+    out = {
+        "sel": (torch.empty((B, N), dtype=torch.float32, device="cuda"),
+                torch.empty((len(rhos), B, N), dtype=torch.uint8, device="cuda"),
+                e32(len(rhos), B), e32(len(rhos), B + 1), e32(len(rhos), total)),
+        "prep": (e32(total), e32(total), torch.empty((total, 1), dtype=torch.int64, device="cuda"),
+                 e32(total), torch.zeros(1, dtype=torch.int32, device="cuda")),
+        "attn_out": torch.empty_like(hd["q"]),
+        "voc": (torch.full((total,), -1, dtype=torch.int32, device="cuda"), e32(total, 8),
+                torch.empty((total, 8), dtype=torch.float32, device="cuda"), None, None),
+        "acc": (e32(B), e32(B), e32(B, N), e32(B), e32(total)),
+        "n_bad": torch.zeros(1, dtype=torch.int32, device="cuda"),
+        "retr": (e32(B, 52), e32(B, 52), e32(B), torch.zeros(1, dtype=torch.int32, device="cuda")),
+    }
+    ws_attn = torch.empty(max(256, lib.tree_verify_attn_workspace_size(B, N, max_prefix, 32, 8, 128, 1)),
+                          dtype=torch.uint8, device="cuda")
+    ws_voc = torch.empty(max(256, lib.vocab_argmax_topk_workspace_size(K, V, 8)), dtype=torch.uint8,
+                         device="cuda")
+    sel = out["sel"]
+
+    def k_dcut():
+        tv.dcut_select(hd["conf"], rhos, outputs=sel)
+
+    def k_prep():
+        tv.tv_tree_prep(hd["parent"], hd["node_off"], hd["prefix_len"], None, N, 1, outputs=out["prep"])
+
+    def k_attn():
+        tv.tree_verify_attn(hd["q"], hd["k_pre"], hd["v_pre"], hd["pre_off"], hd["k_tree"], hd["v_tree"],
+                            hd["node_off"], out["prep"][2], N, max_prefix, node_cnt=sel[2][ri],
+                            out=out["attn_out"], want_lse=False, ws=ws_attn)
+
+    def k_vocab():
+        tv.vocab_argmax_topk(hd["logits"], k=8, rows=K, row_idx=sel[4][ri], out_rows=total,
+                             want_lse=False, want_max=False, ws=ws_voc, outputs=out["voc"])
+
+    def k_accept():
+        tv.accept_longest_path(hd["parent"], hd["tok"], out["voc"][0], hd["node_off"], valid=sel[1][ri],
+                               max_nodes=N, max_depth=D, outputs=out["acc"])
+
+    def k_adj():
+        tv.graft_adj_update(hd["adj"], hd["tok"], out["voc"][1], valid=sel[1][ri], n_bad=out["n_bad"])
+
+    def k_retr():
+        tv.graft_retrieve(hd["adj"], out["acc"][3], stage, *tmpl, 52, out=out["retr"])
+
+    kernels = [("dcut_select", k_dcut, 1), ("tv_tree_prep", k_prep, 1),
+               ("tree_verify_attn", k_attn, 1 + int(ws_attn.numel() > 256)),
+               ("vocab_argmax_topk", k_vocab, 2), ("accept_longest_path", k_accept, 1),
+               ("graft_adj_update", k_adj, 1), ("graft_retrieve", k_retr, 1)]
+
+    def step():
+        for _, f, _ in kernels:
+            f()
+    return step, kernels, out, K
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [l.split(", ") for l in (self.out or "").strip().splitlines() if l.strip()]
+        rows = [r for r in rows if len(r) >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][1]) if rows[0][1].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def time_graph(torch, graphs, n, stream):
+    """Average duration of one replay; ``graphs`` (a graph or a list of graphs
+    over distinct buffers) are replayed round-robin so that a working set
+    smaller than L2 is not re-read from L2."""
+    graphs = graphs if isinstance(graphs, list) else [graphs]
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for i in range(n):
+        graphs[i % len(graphs)].replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / n
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()                                   # first call outside the graph (lazy attributes)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def copies_for(nbytes):
+    """Distinct buffer copies needed for a rotation to exceed L2 twice over."""
+    return max(1, min(32, math.ceil(2 * L2_BYTES / max(1, nbytes))))
+
+
+def attn_bytes(plen, kept, Hq=32, Hkv=8, d=128):
+    """Algorithmic bytes of one attention launch: every request's visible
+    prefix K/V once, plus q, o and the own K/V row of each verified node."""
+    kv = int(plen.sum()) * Hkv * d * 2 * 2
+    return kv + int(kept) * (2 * Hq * d * 2 + 2 * Hkv * d * 2)
+
+
+def row_entry(us, byts, pk, bound="hbm"):
+    gbs = byts / us / 1e3
+    return {"us": round(us, 2), "bytes": int(byts), "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm"], 3),
+            "bound": bound}
+
+
+def measure_rows(tv, torch, pk, stream):
+    """Rows of the path on their own workloads, timed with CUDA-graph replays
+    (inputs rotated across enough copies to exceed L2)."""
+    rows = {}
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5005)
+    V = synth.QWEN3_VOCAB
+    bf = lambda *s, std=2.0: (torch.randn(s, generator=g, device="cuda") * std).to(torch.bfloat16)
+    # a4: alpha on the SpecOPD scoring shape (1024 x 151936, two distributions)
+    lp, lq = bf(1024, V), bf(1024, V)
+    boff = torch.arange(0, 1025, 16, dtype=torch.int32, device="cuda")
+    mtok = torch.randint(0, V, (1024,), generator=g, device="cuda", dtype=torch.int32)
+    ws = torch.empty(tv.load_library().tree_tv_alpha_workspace_size(1024, V), dtype=torch.uint8, device="cuda")
+    o3 = tuple(torch.empty(1024, dtype=torch.float32, device="cuda") for _ in range(3))
+    gr = capture(torch, lambda: tv.tree_tv_alpha(lp, lq, boff, mtok, ws=ws, outputs=o3), stream)
+    rows["tree_tv_alpha[specopd 1024x151936 p,q bf16]"] = row_entry(
+        time_graph(torch, gr, 10, stream) * 1e3, 2 * 1024 * V * 2, pk)
+    del lp, lq, gr
+    # a3: vocab reductions, Graft single request (61 rows) and D-cut batch (1024 rows)
+    for R in (61, 1024):
+        nc = copies_for(R * V * 2)
+        Ls = [bf(R, V) for _ in range(nc)]
+        wsv = torch.empty(tv.load_library().vocab_argmax_topk_workspace_size(R, V, 8), dtype=torch.uint8,
+                          device="cuda")
+        outs = (torch.empty(R, dtype=torch.int32, device="cuda"), torch.empty((R, 8), dtype=torch.int32, device="cuda"),
+                torch.empty((R, 8), dtype=torch.float32, device="cuda"), torch.empty(R, dtype=torch.float32, device="cuda"),
+                torch.empty(R, dtype=torch.float32, device="cuda"))
+        grs = [capture(torch, lambda L=L: tv.vocab_argmax_topk(L, k=8, ws=wsv, outputs=outs), stream) for L in Ls]
+        rows[f"vocab_argmax_topk[{R}x151936 bf16, k=8, max+lse]"] = row_entry(
+            time_graph(torch, grs, 10 * nc, stream) * 1e3, R * V * 2, pk)
+        del Ls, grs
+    # a9: BlockPilot MLP (W1 151936 x 2048 bf16 = 622 MB)
+    W1, W2, last = bf(V, 2048, std=0.02), bf(2048, 7, std=0.02), bf(8, V)
+    lse = tv.vocab_argmax_topk(last, k=0)[4]
+    wsm = torch.empty(tv.load_library().blockpilot_mlp_workspace_size(8, V, 2048), dtype=torch.uint8, device="cuda")
+    om = (torch.empty((8, 7), dtype=torch.float32, device="cuda"), torch.empty(8, dtype=torch.int32, device="cuda"),
+          torch.empty(8, dtype=torch.int32, device="cuda"))
+    gr = capture(torch, lambda: tv.blockpilot_mlp(last, lse, W1, W2, ws=wsm, outputs=om), stream)
+    rows["blockpilot_mlp[8x151936->2048->7]"] = row_entry(
+        time_graph(torch, gr, 10, stream) * 1e3, V * 2048 * 2 + 8 * V * 2, pk)
+    del W1, gr
+    # a6 bulk form: whole-table update of 151936 rows from a [151936, 8] top-k array
+    nbytes = V * 4 + 2 * V * 8 * 4
+    nc = copies_for(nbytes)
+    sets = [(torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32),
+             torch.randperm(V, device="cuda", generator=g).to(torch.int32),
+             torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32)) for _ in range(nc)]
+    nb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb), stream) for a, t, k in sets]
+    rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
+        time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
+    return rows
+
+
+def gpu_arm(args):
+    import torch
+    import speculative_decoding_tree_02_gb300 as tv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    pk = peaks()
+    tv.load_library()
+
+    d = synth.dcut_batch(step=0)
+    plen = d["prefix_len"]
+    hd = {k: to_dev(d[k], torch) for k in ("conf", "parent", "tok", "node_off", "pre_off", "prefix_len",
+                                           "q", "k_pre", "v_pre", "k_tree", "v_tree", "logits")}
+    hd["adj"] = to_dev(synth.successor_table(3), torch)
+    hd.update(B=d["B"], D=d["D"], max_prefix=int(plen.max()))
+    stream = torch.cuda.Stream()
+    step, kernels, out, K = make_step(tv, torch, hd, args.rho)
+    launches_per_step = sum(n for _, _, n in kernels)
+
+    # graph of the whole step
+    g_step = capture(torch, step, stream)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g_step.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * K / (ms_step / 1e3)
+
+    # per-kernel graphs on the same buffers: average launch duration of each kernel
+    per_kernel = {}
+    for name, f, _ in kernels:
+        gk = capture(torch, f, stream)
+        per_kernel[name] = time_graph(torch, gk, max(5, args.steps // 2), stream)
+    a_bytes = attn_bytes(plen, K)           # |keep| = K exactly
+    a_ms = per_kernel["tree_verify_attn"]
+    traffic = load_traffic("tree_verify_attn", WORKLOAD)
+    roofline = {"kernel": "tree_verify_attn", "bound": "hbm", "achieved": a_bytes / a_ms / 1e6,
+                "peak": pk["hbm"], "unit": "GB/s", "frac": a_bytes / a_ms / 1e6 / pk["hbm"],
+                "traffic": traffic, "algorithmic_bytes": a_bytes, "launch_us": a_ms * 1e3,
+                "peak_source": f"{pk['src']} (MEASURED_PEAKS.json hbm_gbs, burst)"}
+    v_bytes = K * synth.QWEN3_VOCAB * 2
+    kern_json = {n: {"us": round(v * 1e3, 2)} for n, v in per_kernel.items()}
+    kern_json["vocab_argmax_topk"].update(gbs=round(v_bytes / per_kernel["vocab_argmax_topk"] / 1e6, 1),
+                                          frac=round(v_bytes / per_kernel["vocab_argmax_topk"] / 1e6 / pk["hbm"], 3))
+    kern_json["tree_verify_attn"].update(gbs=round(roofline["achieved"], 1), frac=round(roofline["frac"], 3))
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of the results
+    step_inputs = ("conf", "parent", "tok", "q", "k_tree", "v_tree", "logits")
+    pinned = {k: to_dev(d[k], torch, pin=True) for k in step_inputs}
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in step_inputs)
+    res_host = {k: torch.empty(s, dtype=torch.int32).pin_memory() for k, s in
+                (("accept_len", (64,)), ("bonus", (64,)), ("path", (64, 16)), ("rtok", (64, 52)))}
+    d2h = sum(t.numel() * 4 for t in res_host.values())
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k in step_inputs:
+                hd[k].copy_(pinned[k], non_blocking=True)
+            g_step.replay()
+            res_host["accept_len"].copy_(out["acc"][0], non_blocking=True)
+            res_host["bonus"].copy_(out["acc"][3], non_blocking=True)
+            res_host["path"].copy_(out["acc"][2], non_blocking=True)
+            res_host["rtok"].copy_(out["retr"][0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host = time.perf_counter()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host
+    e2e_ms = max(e0.elapsed_time(e1), t_host * 1e3) / n_e2e
+    e2e = {"value": world * K / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    rows = None
+    if not args.no_rows and rank == 0:
+        rows = measure_rows(tv, torch, pk, stream)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64; shapes of the D-cut bs=64 workload)",
+            "config": config_dict(args.rho, world), "roofline": roofline, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "kernels": kern_json,
+            "clocks": clk.summary()}
+    if rows:
+        line["rows"] = rows
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = run_cpu_oracle(d, args.rho, steps=3, warmup=0, budget_s=20.0)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the kernel as it is now (source hash match); else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        t = json.load(open(p)).get(f"{kernel}@{workload}")
+    except (ValueError, OSError):
+        return None
+    if not t:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "speculative_decoding_tree_02_gb300", "csrc", t["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    return t["bytes_per_launch"] if h == t.get("source_sha") else None
+
+
+def reference_arm(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    d = synth.dcut_batch(step=0)
+    v, cores, sample, sec = run_cpu_oracle(d, args.rho, args.steps, args.warmup, args.ref_budget_s)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64; shapes of the D-cut bs=64 workload)",
+            "config": config_dict(args.rho, world), "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

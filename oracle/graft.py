@@ -95,3 +95,14 @@ def retrieve(adj, root_tok, stage, tparent, trank, tmpl_off, max_slots):
             rpar[b, s] = p
         nslots[b] = s1 - s0
     return rtok, rpar, nslots
+
+
+def assemble_hybrid(parent_draft, tparent_stage):
+    """Hybrid tree = kept draft nodes (node 0 is the root) followed by the
+    retrieval slots; a slot whose template parent is -1 hangs off the root,
+    any other slot off the node that holds its template parent."""
+    nd = len(parent_draft)
+    parent = list(int(p) for p in parent_draft)
+    for p in tparent_stage:
+        parent.append(0 if p < 0 else nd + int(p))
+    return np.array(parent, np.int32)

@@ -1,0 +1,82 @@
+// tree_verify_attn entry point: host validation, workspace layout, dispatch.
+#include "attn.cuh"
+
+namespace {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  int n_split;
+  size_t o_bytes, ml_bytes, total;
+};
+
+WsLayout ws_layout(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int d) {
+  WsLayout w{};
+  w.n_split = tv::attn_simt_splits(B, max_nodes, max_prefix, Hq, Hkv, sm_count());
+  if (w.n_split <= 1) return w;
+  const size_t rows = static_cast<size_t>(w.n_split) * B * max_nodes * Hq;
+  w.o_bytes = align256(rows * d * sizeof(float));
+  w.ml_bytes = align256(rows * sizeof(float2));
+  w.total = w.o_bytes + w.ml_bytes;
+  return w;
+}
+
+bool shape_ok(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int d) {
+  return B >= 0 && max_nodes >= 0 && max_prefix >= 0 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0 &&
+         (d == 64 || d == 128);
+}
+
+}  // namespace
+
+TV_API size_t tree_verify_attn_workspace_size(int B, int max_nodes, int max_prefix, int Hq,
+                                              int Hkv, int d, int dtype) {
+  (void)dtype;
+  if (!shape_ok(B, max_nodes, max_prefix, Hq, Hkv, d) || B == 0 || max_nodes == 0) return 0;
+  return ws_layout(B, max_nodes, max_prefix, Hq, Hkv, d).total;
+}
+
+TV_API int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre,
+                            const int32_t* pre_off, const void* k_tree, const void* v_tree,
+                            const int32_t* node_off, const int32_t* node_cnt, const uint64_t* anc,
+                            int anc_words, const int32_t* vis_prefix, int B, int max_nodes,
+                            int max_prefix, int Hq, int Hkv, int d, int dtype, float scale,
+                            void* out, float* lse, void* ws, size_t ws_bytes, tv_stream_t stream) {
+  if (B < 0 || max_nodes < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0) return TV_EINVAL;
+  if (Hq % Hkv != 0) return TV_EINVAL;
+  if (d != 64 && d != 128) return TV_EUNSUPPORTED;
+  if (Hq / Hkv > 64) return TV_EUNSUPPORTED;
+  if (dtype != TV_F32 && dtype != TV_BF16) return TV_EINVAL;
+  if (max_nodes > TV_MAX_NODES) return TV_EUNSUPPORTED;
+  if (anc_words < (max_nodes + 63) / 64 || anc_words < 1) return TV_EINVAL;
+  if (!(scale == scale)) return TV_EINVAL;
+  if (B == 0 || max_nodes == 0) return TV_OK;
+  if (!q || !pre_off || !k_tree || !v_tree || !node_off || !anc || !out) return TV_EINVAL;
+  if (max_prefix > 0 && (!k_pre || !v_pre)) return TV_EINVAL;
+  if (static_cast<long long>(B) * Hkv > 65535) return TV_EUNSUPPORTED;
+  // 16-byte rows for the vector loads
+  const void* ptrs[] = {q, k_tree, v_tree, out, k_pre, v_pre};
+  for (const void* ptr : ptrs)
+    if (ptr && !tv::aligned(ptr, 16)) return TV_EINVAL;
+  const WsLayout w = ws_layout(B, max_nodes, max_prefix, Hq, Hkv, d);
+  if (w.total > 0 && (!ws || ws_bytes < w.total || !tv::aligned(ws, 256))) return TV_EWORKSPACE;
+
+  tv::AttnParams p{};
+  p.q = q; p.k_pre = k_pre; p.v_pre = v_pre; p.pre_off = pre_off;
+  p.k_tree = k_tree; p.v_tree = v_tree; p.node_off = node_off; p.node_cnt = node_cnt;
+  p.anc = anc; p.vis_prefix = vis_prefix; p.out = out; p.lse = lse;
+  p.anc_words = anc_words; p.B = B; p.max_nodes = max_nodes; p.max_prefix = max_prefix;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.dtype = dtype; p.scale = scale; p.n_split = w.n_split;
+  if (w.n_split > 1) {
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + w.o_bytes);
+  }
+  return tv::attn_simt(p, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -262,6 +262,12 @@ def dcut_batch(step: int = 0, B: int = 64, D: int = 15, P_min: int = 512, P_max:
     return out
 
 
+def successor_table(workload: int, V: int = QWEN3_VOCAB, k: int = 8) -> np.ndarray:
+    """Initial V x k successor table with uniform random entries (the tables
+    start untrained: no warm-up corpus is available)."""
+    return make_rng(workload, 777_777).integers(0, V, (V, k), dtype=np.int32)
+
+
 # ---------------------------------------------------------------------------
 # workload 4: BlockPilot block-size sweep
 # ---------------------------------------------------------------------------
