@@ -44,8 +44,8 @@ WORKLOAD = "dcut_batch_bs64"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--rho", type=float, default=0.5, help="D-cut budget ratio verified per step")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -244,7 +244,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -280,10 +280,11 @@ def time_graph(torch, graphs, n, stream):
     graphs = graphs if isinstance(graphs, list) else [graphs]
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    s.record(stream)
-    for i in range(n):
-        graphs[i % len(graphs)].replay()
-    e.record(stream)
+    with torch.cuda.stream(stream):            # replay() launches on the current stream
+        s.record(stream)
+        for i in range(n):
+            graphs[i % len(graphs)].replay()
+        e.record(stream)
     torch.cuda.synchronize()
     return s.elapsed_time(e) / n
 
@@ -398,13 +399,15 @@ def gpu_arm(args):
 
     # graph of the whole step
     g_step = capture(torch, step, stream)
-    for _ in range(args.warmup):
-        g_step.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_step.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
+        time.sleep(0.3)                         # let the sampler start before the timed region
         torch.cuda.synchronize()
         ev0.record(stream)
         for _ in range(args.steps):
