@@ -20,7 +20,7 @@ import torch
 from .templates import stage_templates, assemble_hybrid  # noqa: F401  (host-side template data)
 
 __all__ = [
-    "TVError", "lib", "tv_tree_prep", "tree_verify_attn", "vocab_argmax_topk", "tree_tv_alpha",
+    "TVError", "lib", "tv_tree_prep", "tree_verify_attn", "vocab_argmax_topk", "vocab_argmax_topk_noalloc", "tree_tv_alpha",
     "accept_longest_path", "graft_adj_update", "graft_retrieve", "dcut_select", "blockpilot_mlp",
     "stage_templates", "assemble_hybrid", "LIB_PATH", "load_library", "EXPORTS",
 ]
@@ -39,6 +39,7 @@ _SIGS = {
                               _F, _P, _P, _P, _SZ, _P]),
     "vocab_argmax_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "vocab_argmax_topk": (_I, [_P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "vocab_argmax_topk_noalloc": (_I, [_P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _P]),
     "tree_tv_alpha_workspace_size": (_SZ, [_I, _I]),
     "tree_tv_alpha": (_I, [_P, _P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "accept_longest_path": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -192,6 +193,19 @@ def vocab_argmax_topk(logits, k=8, rows=None, row_idx=None, out_rows=None, want_
         _ptr(logits), dt, rows, V, logits.stride(0), _ptr(row_idx), k, _ptr(argmax), _ptr(tki), _ptr(tkv),
         _ptr(rmax), _ptr(rlse), _ptr(ws), ws.numel(), _stream()))
     return argmax, tki, tkv, rmax, rlse
+
+
+def vocab_argmax_topk_noalloc(logits, argmax, topk_idx=None, topk_val=None, row_max=None,
+                              row_lse=None, k=8, rows=None, row_idx=None):
+    """vocab_argmax_topk without a workspace (fixed device scratch inside the
+    library, see include/tv.h); the caller passes preallocated outputs."""
+    R, V = logits.shape
+    if rows is None:
+        rows = row_idx.numel() if row_idx is not None else R
+    _check("vocab_argmax_topk_noalloc", load_library().vocab_argmax_topk_noalloc(
+        _ptr(logits), _dtype_code(logits), rows, V, logits.stride(0), _ptr(row_idx), k, _ptr(argmax),
+        _ptr(topk_idx), _ptr(topk_val), _ptr(row_max), _ptr(row_lse), _stream()))
+    return argmax, topk_idx, topk_val, row_max, row_lse
 
 
 def tree_tv_alpha(lp, lq, branch_off=None, mass_tok=None, ws=None, outputs=None):

@@ -382,3 +382,68 @@ TV_API int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int
   return tv::vocab_dispatch(static_cast<const float*>(logits), rows, V, ld, row_idx, k, argmax,
                             topk_idx, topk_val, row_max, row_lse, ws, st);
 }
+
+// ---------------------------------------------------------------------------
+// vocab_argmax_topk_noalloc: the same reduction for callers that cannot
+// allocate device memory.  Its chunk partials live in a fixed file-scope
+// device array instead of a caller workspace.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;   // TV_NOALLOC_SCRATCH_BYTES
+constexpr int kNoallocMaxDevices = 64;
+
+// Loaded with the library on every GPU that uses it and kept until exit.
+static __device__ __align__(256) unsigned char g_vocab_scratch[kNoallocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kNoallocMaxDevices] = {};
+
+// Device address of g_vocab_scratch on the current device, looked up once per
+// device (host code only knows the symbol's host-side shadow, not its address).
+void* scratch_address(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
+    *status = TV_ECUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_vocab_scratch) != cudaSuccess || !p) {
+      *status = TV_ECUDA;
+      return nullptr;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *status = TV_OK;
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+TV_API int vocab_argmax_topk_noalloc(const void* logits, int dtype, int rows, int V, int64_t ld,
+                                     const int32_t* row_idx, int k, int32_t* argmax,
+                                     int32_t* topk_idx, float* topk_val, float* row_max,
+                                     float* row_lse, tv_stream_t stream) {
+  if (rows < 0 || V <= 0 || k < 0 || ld < V) return TV_EINVAL;
+  if (k > TV_MAX_TOPK) return TV_EUNSUPPORTED;
+  if (k > V) return TV_EINVAL;
+  if (dtype != TV_F32 && dtype != TV_BF16) return TV_EINVAL;
+  if (rows == 0) return TV_OK;
+  if (!logits || !argmax) return TV_EINVAL;
+  if (k > 0 && !topk_idx && !topk_val) return TV_EINVAL;
+  if (rows > 65535) return TV_EUNSUPPORTED;
+  if (vocab_argmax_topk_workspace_size(rows, V, k) > kNoallocScratchBytes) return TV_EWORKSPACE;
+  int st = TV_OK;
+  void* scratch = scratch_address(&st);
+  if (st != TV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == TV_BF16)
+    return tv::vocab_dispatch(static_cast<const uint16_t*>(logits), rows, V, ld, row_idx, k, argmax,
+                              topk_idx, topk_val, row_max, row_lse, scratch, s);
+  return tv::vocab_dispatch(static_cast<const float*>(logits), rows, V, ld, row_idx, k, argmax,
+                            topk_idx, topk_val, row_max, row_lse, scratch, s);
+}
