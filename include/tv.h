@@ -112,20 +112,28 @@ int tv_tree_prep(const int32_t* parent, const int32_t* node_off, const int32_t* 
  *   anc      uint64 [n, anc_words] from tv_tree_prep
  *   vis_prefix int32 [n] or NULL (= whole prefix); clamped to the prefix
  *   max_nodes, max_prefix  upper bounds over requests (launch geometry)
+ *   total_nodes   rows of q / k_tree / v_tree (= node_off[B]; the tensor size)
+ *   total_prefix  rows of k_pre / v_pre (>= max_prefix)
  *   d ∈ {64, 128}; Hq % Hkv == 0; scale is applied to q.k
+ * bf16 with d = 128 (and Hq/Hkv dividing 128) runs on the tensor cores
+ * (tcgen05 MMA, TMA-loaded K/V tiles, TMEM accumulators); other shapes on a
+ * SIMT kernel with fp32 arithmetic.
  * Outputs: out [n, Hq, d] dtype; lse float [n, Hq] (natural log of the sum of
  *   exp(scale*q.k) over visible keys) or NULL.
- * Workspace: tree_verify_attn_workspace_size(...) bytes (partial results of
- *   the key-split path), 256-byte aligned.
+ * Workspace: tree_verify_attn_workspace_size(...) bytes, 256-byte aligned.
+ *   Its first int32 is a status word, set to 0 by the call and to a nonzero
+ *   code if a pipeline wait inside the tensor-core kernel ran out (about 2 s;
+ *   the outputs are then invalid).  The rest holds the key-split partials.
  * -------------------------------------------------------------------------- */
 size_t tree_verify_attn_workspace_size(int B, int max_nodes, int max_prefix, int Hq, int Hkv,
                                        int d, int dtype);
 int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre, const int32_t* pre_off,
                      const void* k_tree, const void* v_tree, const int32_t* node_off,
                      const int32_t* node_cnt, const uint64_t* anc, int anc_words,
-                     const int32_t* vis_prefix, int B, int max_nodes, int max_prefix, int Hq,
-                     int Hkv, int d, int dtype, float scale, void* out, float* lse, void* ws,
-                     size_t ws_bytes, tv_stream_t stream);
+                     const int32_t* vis_prefix, int B, int max_nodes, int max_prefix,
+                     long long total_nodes, long long total_prefix, int Hq, int Hkv, int d,
+                     int dtype, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                     tv_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * vocab_argmax_topk — per-row reductions over next-token logits.

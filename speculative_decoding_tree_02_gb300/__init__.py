@@ -35,8 +35,8 @@ _SIGS = {
     "tv_version": (_I, []),
     "tv_tree_prep": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "tree_verify_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
-    "tree_verify_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I,
-                              _F, _P, _P, _P, _SZ, _P]),
+    "tree_verify_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, ctypes.c_longlong,
+                              ctypes.c_longlong, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "vocab_argmax_topk_workspace_size": (_SZ, [_I, _I, _I]),
     "vocab_argmax_topk": (_I, [_P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "vocab_argmax_topk_noalloc": (_I, [_P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _P]),
@@ -162,8 +162,9 @@ def tree_verify_attn(q, k_pre, v_pre, pre_off, k_tree, v_tree, node_off, anc, ma
         ws = _ws(need, q.device)
     _check("tree_verify_attn", load_library().tree_verify_attn(
         _ptr(q), _ptr(k_pre), _ptr(v_pre), _ptr(pre_off), _ptr(k_tree), _ptr(v_tree), _ptr(node_off),
-        _ptr(node_cnt), _ptr(anc), anc.shape[1], _ptr(vis_prefix), B, max_nodes, max_prefix, Hq, Hkv, d,
-        dt, float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream()))
+        _ptr(node_cnt), _ptr(anc), anc.shape[1], _ptr(vis_prefix), B, max_nodes, max_prefix, n,
+        k_pre.shape[0] if k_pre is not None else 0, Hq, Hkv, d, dt, float(scale), _ptr(out), _ptr(lse),
+        _ptr(ws), ws.numel(), _stream()))
     return out, lse
 
 

@@ -30,5 +30,12 @@ struct AttnParams {
 
 int attn_simt(const AttnParams& p, cudaStream_t st);
 int attn_simt_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm);
+// Merges the key-split partials in split order (shared by both paths).
+int attn_combine(const AttnParams& p, cudaStream_t st);
+
+// Tensor-core path: bf16, head_dim 128, Hq/Hkv dividing 128.
+bool attn_tc_supported(int dtype, int d, int Hq, int Hkv);
+int attn_tc_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm);
+int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st);
 
 }  // namespace tv

@@ -296,9 +296,18 @@ int attn_simt_launch(const AttnParams& p, cudaStream_t st) {
   const int tiles = (p.max_nodes + nq - 1) / nq;
   dim3 grid(p.n_split, tiles, p.B * p.Hkv);
   attn_simt_kernel<T, D><<<grid, kSThreads, 0, st>>>(p);
-  if (p.n_split > 1) {
-    dim3 g2(p.max_nodes, p.B);
-    attn_combine_kernel<T, D><<<g2, 256, 0, st>>>(p);
+  if (p.n_split > 1) return attn_combine(p, st);
+  return launch_status();
+}
+
+int attn_combine(const AttnParams& p, cudaStream_t st) {
+  dim3 g2(p.max_nodes, p.B);
+  if (p.dtype == TV_BF16) {
+    if (p.d == 128) attn_combine_kernel<uint16_t, 128><<<g2, 256, 0, st>>>(p);
+    else attn_combine_kernel<uint16_t, 64><<<g2, 256, 0, st>>>(p);
+  } else {
+    if (p.d == 128) attn_combine_kernel<float, 128><<<g2, 256, 0, st>>>(p);
+    else attn_combine_kernel<float, 64><<<g2, 256, 0, st>>>(p);
   }
   return launch_status();
 }

@@ -456,3 +456,39 @@ def test_blockpilot_zero_weights(tv):
     z, choice, bsize = tv.blockpilot_mlp(L, lse, W1, W2, block=16)
     sync()
     assert np.all(host(z) == 0) and np.all(host(choice) == 0) and np.all(host(bsize) == 13)
+
+
+def test_attn_simt_path_on_bf16_in_subprocess(tv):
+    """bf16 / head_dim 128 normally runs on the tensor cores; the SIMT kernel
+    for the same shapes is checked in a process with TV_ATTN_PATH=simt."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); sys.path.insert(0, '.');"
+        "import test_gpu_kernels as t, synth, speculative_decoding_tree_02_gb300 as tv;"
+        "t.run_attn(tv, synth.dcut_batch(B=6, P_min=1, P_max=700, V=64),"
+        " node_cnt=__import__('numpy').array([16, 1, 5, 16, 9, 3], 'int32'));"
+        "st = synth.graft_static(V=1000); d = synth.graft_step(3, st); tp, tr, off = tv.stage_templates();"
+        "d['parent'] = tv.assemble_hybrid(d['parent_draft'], tp[off[d['stage']]:off[d['stage'] + 1]]);"
+        "t.run_attn(tv, d); print('simt ok')")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, TV_ATTN_PATH="simt")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "simt ok" in r.stdout, r.stderr[-3000:]
+
+
+def test_attn_status_word_clear(tv):
+    """The tensor-core kernel reports no pipeline timeout on a normal call."""
+    d = synth.dcut_batch(B=4, P_min=100, P_max=900, V=64)
+    off, pre_off = d["node_off"], d["pre_off"]
+    plen = np.diff(pre_off).astype(np.int32)
+    _, _, anc, _, _ = tv.tv_tree_prep(dev(d["parent"]), dev(off), dev(plen), None, 16, 1)
+    need = tv.load_library().tree_verify_attn_workspace_size(4, 16, int(plen.max()), 32, 8, 128, 1)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ws[:4] = 7
+    tv.tree_verify_attn(dev(d["q"]), dev(d["k_pre"]), dev(d["v_pre"]), dev(pre_off), dev(d["k_tree"]),
+                        dev(d["v_tree"]), dev(off), anc, 16, int(plen.max()), ws=ws)
+    sync()
+    assert int(ws[:4].view(torch.int32).item()) == 0

@@ -68,7 +68,7 @@ def test_host_validation_rejects_bad_arguments_without_launching(built_lib):
     assert lib.vocab_argmax_topk(ctypes.c_void_p(16), 1, 4, 100, 100, null, 8, ctypes.c_void_p(16),
                                  ctypes.c_void_p(16), null, null, null, null, 0, null) == -4
     # head dim not supported
-    assert lib.tree_verify_attn(*([ctypes.c_void_p(256)] * 9), 1, null, 1, 8, 8, 4, 1, 96, 1,
+    assert lib.tree_verify_attn(*([ctypes.c_void_p(256)] * 9), 1, null, 1, 8, 8, 8, 8, 4, 1, 96, 1,
                                 ctypes.c_float(0.1), ctypes.c_void_p(256), null, null, 0, null) == -2
     # too many nodes per request
     assert lib.tv_tree_prep(*([ctypes.c_void_p(256)] * 4), 1, 2000, 32, *([ctypes.c_void_p(256)] * 5),
