@@ -114,7 +114,7 @@ int tv_tree_prep(const int32_t* parent, const int32_t* node_off, const int32_t* 
  *   max_nodes, max_prefix  upper bounds over requests (launch geometry)
  *   total_nodes   rows of q / k_tree / v_tree (= node_off[B]; the tensor size)
  *   total_prefix  rows of k_pre / v_pre (>= max_prefix)
- *   d ∈ {64, 128}; Hq % Hkv == 0; scale is applied to q.k
+ *   d ∈ {64, 128}; Hq % Hkv == 0; scale > 0 is applied to q.k
  * bf16 with d = 128 (and Hq/Hkv dividing 128) runs on the tensor cores
  * (tcgen05 MMA, TMA-loaded K/V tiles, TMEM accumulators); other shapes on a
  * SIMT kernel with fp32 arithmetic.
@@ -173,8 +173,8 @@ int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld
  * holds until the process exits.  Arguments and outputs are those of
  * vocab_argmax_topk; the caller still provides the inputs and outputs.
  *   - Sizes whose scratch need (vocab_argmax_topk_workspace_size) exceeds
- *     TV_NOALLOC_SCRATCH_BYTES are rejected with TV_EWORKSPACE (for V = 151936
- *     and k <= 8: up to 6132 rows).
+ *     TV_NOALLOC_SCRATCH_BYTES are rejected with TV_EWORKSPACE (for V = 151936:
+ *     up to 1623 rows).
  *   - The first call on a device looks up the array's device address (one
  *     runtime query, no allocation); make that first call before any stream
  *     capture on that device.

@@ -78,7 +78,7 @@ TV_API int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre,
   if (dtype != TV_F32 && dtype != TV_BF16) return TV_EINVAL;
   if (max_nodes > TV_MAX_NODES) return TV_EUNSUPPORTED;
   if (anc_words < (max_nodes + 63) / 64 || anc_words < 1) return TV_EINVAL;
-  if (!(scale == scale)) return TV_EINVAL;
+  if (!(scale > 0.f)) return TV_EINVAL;   // positive and not NaN
   if (B == 0 || max_nodes == 0 || total_nodes == 0) return TV_OK;
   if (max_prefix > total_prefix) return TV_EINVAL;
   if (!q || !pre_off || !k_tree || !v_tree || !node_off || !anc || !out) return TV_EINVAL;

@@ -3,18 +3,24 @@
 // SpecOPD page §02 proposal-tree scoring with the ancestor mask).
 //
 // One CTA = (request, KV head, tile of 128 query rows = 128/g nodes x g heads,
-// split of the prefix keys).  Keys stream in blocks of 128:
-//   warp 0   TMA producer: Q once, then K and V blocks into a 2-stage ring
-//            (cp.async.bulk.tensor, 128-byte swizzle).
-//   warp 1   MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
-//            accumulator (128 x 128 fp32), then O += P V into a TMEM
+// split of the prefix keys).  Keys stream in blocks of 64:
+//   warp 0   TMA producer: Q once, then K and V blocks into separate 5-stage
+//            rings (cp.async.bulk.tensor, 128-byte swizzle): a K slot is
+//            reused once S of its block is done, a V slot once PV is.
+//   warp 1   MMA issuer (one thread, event loop): S = Q K^T into a double-buffered TMEM
+//            accumulator (128 x 64 fp32), then O += P V into a TMEM
 //            accumulator (128 x 128 fp32); tcgen05.commit signals mbarriers.
-//            Also owns the TMEM allocation.
+//            Also owns the TMEM allocation (256 columns).
 //   warps 2-5 softmax, one thread per query row (its TMEM lane): load S,
 //            apply the ancestor/prefix mask in registers, online base-2
 //            softmax with lazy rescaling (O is rescaled in TMEM only when the
 //            running max grows by more than 2^8), write P as bf16 into shared
 //            memory in the UMMA K-major layout, and finally normalise O.
+//            A warp none of whose rows is a live query keeps the barrier
+//            protocol but skips the TMEM loads and the arithmetic.
+// P is double-buffered: the softmax of block j waits only for PV(j-2) (its
+// buffer), and for PV(j-1) only in the rare block where O must be rescaled,
+// so the tensor core and the softmax warps overlap across blocks.
 // S for block j+1 is computed while the softmax warps work on block j.
 // Every wait is bounded (2 s): on expiry the CTA records an error code in the
 // workspace status word and stops; TMEM is always released.
@@ -30,26 +36,46 @@
 namespace tv {
 namespace tc {
 
-constexpr int kRows = 128;
-constexpr int kBlk = 128;
+constexpr int kRows = 128;                   // MMA M: TMEM lanes
+constexpr int kBlk = 64;                     // keys per block
 constexpr int kD = 128;
-constexpr int kThreads = 192;
-constexpr uint32_t kHalf = 16384;            // one 64-column half of a 128 x 128 bf16 tile
-constexpr uint32_t kTile = 2 * kHalf;        // 32 KB
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kQOff + kTile;    // 2 stages
-constexpr uint32_t kVOff = kKOff + 2 * kTile;
-constexpr uint32_t kPOff = kVOff + 2 * kTile;
-constexpr uint32_t kBarOff = kPOff + kTile;
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // barriers + 1 KB alignment slack
+constexpr uint32_t kKVHalf = 8192;           // 64 keys x 64 dims bf16
+constexpr uint32_t kTmemCols = 256;          // S0 | S1 | O
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-// mbarrier slots (8 bytes each) at kBarOff
-enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_FREE = 9, P_FULL = 11,
-           O_READY = 12, DRAIN = 13, N_BARS = 14 };
-constexpr uint32_t kTmemSlot = kBarOff + 8 * 16;
-constexpr uint32_t kAbortSlot = kTmemSlot + 4;
-constexpr uint32_t kRedSlot = kTmemSlot + 16;   // [6 warps][3] ints
+// Shared-memory layout for LIVE query rows per tile (128, or 64 when a
+// request's nodes x heads fit in 64 rows).  The MMA always has M = 128; with
+// LIVE = 64 its rows 64..127 read the bytes that follow Q or P (still inside
+// the CTA's shared memory) and the results of those rows are never used.  The
+// 64-row layout is half the size, so two CTAs share an SM.
+template <int LIVE>
+struct Lay {
+  // warp roles: softmax warps own TMEM lanes 32*(warp%4)..; with 64 live rows
+  // only lanes 0..63 matter, so the CTA is 4 warps (softmax 0-1, TMA 2, MMA 3);
+  // with 128 it is 6 warps (TMA 0, MMA 1, softmax 2-5)
+  static constexpr int kThreads = LIVE == 128 ? 192 : 128;
+  static constexpr int kSoft = LIVE;                     // softmax threads
+  static constexpr int kTmaWarp = LIVE == 128 ? 0 : 2;
+  static constexpr int kMmaWarp = LIVE == 128 ? 1 : 3;
+  static __device__ __forceinline__ bool soft_warp(int w) { return LIVE == 128 ? w >= 2 : w < 2; }
+  static constexpr int kStages = LIVE == 128 ? 5 : 2;   // per ring (K and V)
+  static constexpr uint32_t kQHalf = LIVE * 128;        // LIVE rows x 64 dims
+  static constexpr uint32_t kPBytes = LIVE * 128;       // LIVE rows x 64 keys
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kPOff = 2 * kQHalf;         // two P buffers
+  static constexpr uint32_t kKRingOff = kPOff + 2 * kPBytes;
+  static constexpr uint32_t kVRingOff = kKRingOff + kStages * 2 * kKVHalf;
+  static constexpr uint32_t kBarOff = kVRingOff + kStages * 2 * kKVHalf;
+  static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;   // barriers + 1 KB alignment slack
+  static constexpr uint32_t kTmemSlot = kBarOff + 8 * 32;
+  static constexpr uint32_t kAbortSlot = kTmemSlot + 4;
+  static constexpr uint32_t kRedSlot = kTmemSlot + 8;   // [6 warps][3] ints (72 B)
+  static_assert(kRedSlot + 72 <= kBarOff + 512, "barrier area");
+};
+
+// mbarrier slots (8 bytes each) at kBarOff; K/V arrays sized for 5 stages
+enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 6, K_EMPTY = 11, V_EMPTY = 16, S_FULL = 21, S_FREE = 23,
+           P_FULL = 25, P_FREE = 27, O_READY = 29, DRAIN = 30, N_BARS = 31 };
 
 struct Maps {
   CUtensorMap q, kp, vp, kt, vt;
@@ -78,6 +104,28 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Progress watchdog of the event loops: true while waiting may continue.
+__device__ __forceinline__ bool still_waiting(uint64_t& since, volatile int* abort_flag, int* err, int code) {
+  if (*abort_flag) return false;
+  const uint64_t t = gtime();
+  if (since == 0) since = t;
+  if (t - since <= kTimeoutNs) return true;
+  *abort_flag = 1;
+  if (err) atomicExch(err, code);
+  return false;
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -183,7 +231,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams P) {
+template <int LIVE>
+__global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn_tc_kernel(
+    const __grid_constant__ TcParams P) {
+  using L = Lay<LIVE>;
+  constexpr int kThreads = L::kThreads;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kQHalf = L::kQHalf, kPBytes = L::kPBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
@@ -192,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int split = blockIdx.x, tile = blockIdx.y;
   const int r = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
   const int g = p.Hq / p.Hkv;
-  const int nq = kRows / g;
+  const int nq = LIVE / g;
   const int n0 = p.node_off[r];
   const int N = p.node_off[r + 1] - n0;
   const int cnt = min(p.node_cnt ? min(p.node_cnt[r], N) : N, p.max_nodes);
@@ -201,16 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int pre0 = p.pre_off[r];
   const int Pr = p.pre_off[r + 1] - pre0;
 
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kAbortSlot);
-  int* red = reinterpret_cast<int*>(sm + kRedSlot);
-  auto bar = [&](int i) { return sb + kBarOff + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbortSlot);
+  int* red = reinterpret_cast<int*>(sm + L::kRedSlot);
+  auto bar = [&](int i) { return sb + L::kBarOff + 8u * i; };
 
   // ---- row identity (softmax warps 2..5 own TMEM lanes 32*(warp%4) ..)
-  const bool is_soft = warp >= 2;
+  const bool is_soft = L::soft_warp(warp);
   const int row = 32 * (warp & 3) + lane;
   const int ln = node_first + row / g;
   const int head = kvh * g + row % g;
-  const bool active = is_soft && ln < cnt;
+  const bool active = is_soft && row < LIVE && ln < cnt;
   const int gn = n0 + ln;
   int vis = 0, lowest = 1 << 30;
   if (active) {
@@ -230,23 +284,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t c = 1;
-      if (i == S_FREE || i == S_FREE + 1 || i == P_FULL) c = kRows;
+      if (i == S_FREE || i == S_FREE + 1 || i == P_FULL || i == P_FULL + 1) c = L::kSoft;
       mbar_init(bar(i), c);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == L::kMmaWarp) {
     __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sb + kTmemSlot),
-                 "r"(512u)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sb + L::kTmemSlot),
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + L::kTmemSlot);
   int vmax = 0, tlo = 1 << 30, thi = -1;
   for (int w = 0; w < kThreads / 32; ++w) {
     vmax = max(vmax, red[3 * w]);
@@ -260,80 +314,104 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int ke = min(kb + chunk, vmax);
   const int n_pre = ke > kb ? (ke - kb + kBlk - 1) / kBlk : 0;
   const bool do_tree = (split == p.n_split - 1) && thi >= 0 && tlo <= thi;
-  const int tb = do_tree ? (tlo & ~63) : 0;
+  const int tb = do_tree ? (tlo & ~63) : 0;   // one 64-bit ancestor word per 64-key block
   const int n_tree = do_tree ? (thi + 1 - tb + kBlk - 1) / kBlk : 0;
   const int nblk = n_pre + n_tree;
   int* err = P.err;
 
-  const uint32_t sQ = sb + kQOff, sK = sb + kKOff, sV = sb + kVOff, sP = sb + kPOff;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
+  const uint32_t sQ = sb + L::kQOff, sP = sb + L::kPOff, sK = sb + L::kKRingOff, sV = sb + L::kVRingOff;
+  const uint32_t tS0 = tmem, tO = tmem + 2 * kBlk;
 
   if (nblk > 0) {
-    if (warp == 0) {
-      // ================= TMA producer
+    if (warp == L::kTmaWarp) {
+      // ================= TMA producer (event loop: K and V rings refill independently)
       if (lane == 0) {
-        bool ok = true;
-        mbar_expect_tx(bar(Q_FULL), kTile);
+        mbar_expect_tx(bar(Q_FULL), 2 * kQHalf);
         tma_load_3d(sQ, &P.maps.q, 0, kvh * g, n0 + node_first, bar(Q_FULL));
-        tma_load_3d(sQ + kHalf, &P.maps.q, 64, kvh * g, n0 + node_first, bar(Q_FULL));
-        for (int j = 0; j < nblk && ok; ++j) {
-          const int s = j & 1;
-          if (j >= 2) ok = mbar_wait(bar(KV_EMPTY + s), ((j >> 1) - 1) & 1, abort_flag, err, 1);
-          if (!ok) break;
+        tma_load_3d(sQ + kQHalf, &P.maps.q, 64, kvh * g, n0 + node_first, bar(Q_FULL));
+        // block j: its tensor maps and token coordinate
+        auto where = [&](int j, const CUtensorMap*& mk, const CUtensorMap*& mv) {
           const bool tree = j >= n_pre;
-          const int start = tree ? tb + (j - n_pre) * kBlk : kb + j * kBlk;
-          const int coord = tree ? n0 + start : pre0 + start;
-          const CUtensorMap* mk = tree ? &P.maps.kt : &P.maps.kp;
-          const CUtensorMap* mv = tree ? &P.maps.vt : &P.maps.vp;
-          const uint32_t dk = sK + s * kTile, dv = sV + s * kTile;
-          mbar_expect_tx(bar(K_FULL + s), kTile);
-          tma_load_3d(dk, mk, 0, kvh, coord, bar(K_FULL + s));
-          tma_load_3d(dk + kHalf, mk, 64, kvh, coord, bar(K_FULL + s));
-          mbar_expect_tx(bar(V_FULL + s), kTile);
-          tma_load_3d(dv, mv, 0, kvh, coord, bar(V_FULL + s));
-          tma_load_3d(dv + kHalf, mv, 64, kvh, coord, bar(V_FULL + s));
+          mk = tree ? &P.maps.kt : &P.maps.kp;
+          mv = tree ? &P.maps.vt : &P.maps.vp;
+          return tree ? n0 + tb + (j - n_pre) * kBlk : pre0 + kb + j * kBlk;
+        };
+        int nk = 0, nv = 0;
+        uint64_t since = 0;
+        while (nk < nblk || nv < nblk) {
+          bool prog = false;
+          if (nk < nblk && (nk < kStages || mbar_test(bar(K_EMPTY + nk % kStages), ((nk / kStages) - 1) & 1))) {
+            const CUtensorMap *mk, *mv;
+            const int coord = where(nk, mk, mv);
+            const uint32_t dk = sK + (nk % kStages) * 2 * kKVHalf;
+            mbar_expect_tx(bar(K_FULL + nk % kStages), 2 * kKVHalf);
+            tma_load_3d(dk, mk, 0, kvh, coord, bar(K_FULL + nk % kStages));
+            tma_load_3d(dk + kKVHalf, mk, 64, kvh, coord, bar(K_FULL + nk % kStages));
+            ++nk;
+            prog = true;
+          }
+          if (nv < nk && (nv < kStages || mbar_test(bar(V_EMPTY + nv % kStages), ((nv / kStages) - 1) & 1))) {
+            const CUtensorMap *mk, *mv;
+            const int coord = where(nv, mk, mv);
+            const uint32_t dv = sV + (nv % kStages) * 2 * kKVHalf;
+            mbar_expect_tx(bar(V_FULL + nv % kStages), 2 * kKVHalf);
+            tma_load_3d(dv, mv, 0, kvh, coord, bar(V_FULL + nv % kStages));
+            tma_load_3d(dv + kKVHalf, mv, 64, kvh, coord, bar(V_FULL + nv % kStages));
+            ++nv;
+            prog = true;
+          }
+          if (prog) since = 0;
+          else if (!still_waiting(since, abort_flag, err, 1)) break;
         }
       }
-    } else if (warp == 1) {
-      // ================= MMA issuer
+    } else if (warp == L::kMmaWarp) {
+      // ================= MMA issuer (event loop: S(j) as soon as its K and S
+      // buffer are ready, PV(j) as soon as P(j) and V(j) are; neither waits
+      // behind the other)
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16(kRows, kBlk, 0);
         constexpr uint32_t idO = idesc_bf16(kRows, kD, 1);
         bool ok = mbar_wait(bar(Q_FULL), 0, abort_flag, err, 2);
         tc_fence_after();
-        auto issue_s = [&](int j) -> bool {
-          const int s = j & 1;
-          if (!mbar_wait(bar(K_FULL + s), (j >> 1) & 1, abort_flag, err, 3)) return false;
-          if (j >= 2 && !mbar_wait(bar(S_FREE + s), ((j >> 1) - 1) & 1, abort_flag, err, 4)) return false;
-          tc_fence_after();
-          const uint32_t kbase = sK + s * kTile;
+        int ns = 0, npv = 0;
+        uint64_t since = 0;
+        while (ok && npv < nblk) {
+          bool prog = false;
+          if (ns < nblk && mbar_test(bar(K_FULL + ns % kStages), (ns / kStages) & 1) &&
+              (ns < 2 || mbar_test(bar(S_FREE + (ns & 1)), ((ns >> 1) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kbase = sK + (ns % kStages) * 2 * kKVHalf;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tS0 + 128 * s, sdesc(sQ + off, 16, 1024), sdesc(kbase + off, 16, 1024), idS, kk > 0);
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+              const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+              umma_bf16(tS0 + kBlk * (ns & 1), sdesc(sQ + qo, 16, 1024), sdesc(kbase + ko, 16, 1024), idS, kk > 0);
+            }
+            umma_commit(bar(S_FULL + (ns & 1)));
+            umma_commit(bar(K_EMPTY + ns % kStages));
+            ++ns;
+            prog = true;
           }
-          umma_commit(bar(S_FULL + s));
-          return true;
-        };
-        if (ok) ok = issue_s(0);
-        if (ok && nblk > 1) ok = issue_s(1);
-        for (int j = 0; j < nblk && ok; ++j) {
-          const int s = j & 1;
-          ok = mbar_wait(bar(P_FULL), j & 1, abort_flag, err, 5);
-          if (ok) ok = mbar_wait(bar(V_FULL + s), (j >> 1) & 1, abort_flag, err, 6);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t vbase = sV + s * kTile;
+          if (npv < ns && mbar_test(bar(P_FULL + (npv & 1)), (npv >> 1) & 1) &&
+              mbar_test(bar(V_FULL + npv % kStages), (npv / kStages) & 1)) {
+            tc_fence_after();
+            const uint32_t vbase = sV + (npv % kStages) * 2 * kKVHalf;
+            const uint32_t pbase = sP + (npv & 1) * kPBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;   // P: K-major over keys
-            const uint32_t boff = kk * 2048;                            // V: 16 keys = 2 x 1 KB atoms
-            umma_bf16(tO, sdesc(sP + aoff, 16, 1024), sdesc(vbase + boff, kHalf, 1024), idO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBlk / 16; ++kk) {
+              // P: K-major over the 64 keys (one 128-byte swizzle column); V: MN-major,
+              // 16 keys = two 1 KB atoms, second 64-dim half kKVHalf bytes away
+              umma_bf16(tO, sdesc(pbase + kk * 32, 16, 1024), sdesc(vbase + kk * 2048, kKVHalf, 1024), idO,
+                        (npv > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(bar(P_FREE + (npv & 1)));
+            umma_commit(bar(O_READY));
+            umma_commit(bar(V_EMPTY + npv % kStages));
+            ++npv;
+            prog = true;
           }
-          umma_commit(bar(O_READY));
-          umma_commit(bar(KV_EMPTY + s));
-          if (j + 2 < nblk) ok = issue_s(j + 2);
+          if (prog) since = 0;
+          else if (!still_waiting(since, abort_flag, err, 5)) ok = false;
         }
         // drain: every MMA issued above has completed before TMEM is released
         umma_commit(bar(DRAIN));
@@ -343,142 +421,173 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       // ================= softmax warps
       const float c2 = p.scale * kLog2e;
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const bool warp_live = __any_sync(0xffffffffu, active);
+      uint8_t* prow = sm + L::kPOff + row * 128;
+      if (!warp_live && row < LIVE) {
+        // rows that are no live query: P stays zero in both buffers for the whole CTA
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          *reinterpret_cast<uint4*>(prow + (c8 << 4)) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(prow + kPBytes + (c8 << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < nblk && ok; ++j) {
-        const int s = j & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(S_FULL + s), (j >> 1) & 1, abort_flag, err, 8));
+        const int sb2 = j & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(S_FULL + sb2), (j >> 1) & 1, abort_flag, err, 8));
         if (!ok) break;
         tc_fence_after();
-        uint32_t xr[4][32];
+        uint32_t xr[2][32];
+        if (warp_live) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS0 + 128 * s + lane_off + 32 * q, xr[q]);
-        tmem_ld_wait();
+          for (int q = 0; q < 2; ++q) tmem_ld32(tS0 + kBlk * sb2 + lane_off + 32 * q, xr[q]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pin(xr[q][c]);
-        tc_fence_before();
-        mbar_arrive(bar(S_FREE + s));
-
-        // visibility of the 128 keys of block j for this row
-        uint32_t vm[4] = {0u, 0u, 0u, 0u};
-        if (active) {
-          if (j < n_pre) {
-            const int start = kb + j * kBlk;
-            const int nv = min(vis, ke) - start;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int t = nv - 32 * q;
-              vm[q] = t >= 32 ? 0xffffffffu : (t > 0 ? (1u << t) - 1u : 0u);
-            }
-          } else {
-            const int start = tb + (j - n_pre) * kBlk;
-            const int w = start >> 6;
-            const uint64_t a0 = w < p.anc_words ? p.anc[static_cast<int64_t>(gn) * p.anc_words + w] : 0ull;
-            const uint64_t a1 = w + 1 < p.anc_words ? p.anc[static_cast<int64_t>(gn) * p.anc_words + w + 1] : 0ull;
-            vm[0] = static_cast<uint32_t>(a0);
-            vm[1] = static_cast<uint32_t>(a0 >> 32);
-            vm[2] = static_cast<uint32_t>(a1);
-            vm[3] = static_cast<uint32_t>(a1 >> 32);
-          }
+            for (int c = 0; c < 32; ++c) pin(xr[q][c]);
         }
-        float mloc = -INFINITY;
+        tc_fence_before();
+        mbar_arrive(bar(S_FREE + sb2));
+
+        float corr = 1.f, rs = 0.f;
+        bool rescale_row = false;
+        uint32_t pk[2][16];
+        if (warp_live) {
+          // visibility of the 64 keys of block j for this row; full = all visible
+          uint32_t vm[2] = {0u, 0u};
+          if (active) {
+            if (j < n_pre) {
+              const int nv = min(vis, ke) - (kb + j * kBlk);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float x = ((vm[q] >> c) & 1u) ? __uint_as_float(xr[q][c]) * c2 : -INFINITY;
-            xr[q][c] = __float_as_uint(x);
-            mloc = fmaxf(mloc, x);
+              for (int q = 0; q < 2; ++q) {
+                const int t = nv - 32 * q;
+                vm[q] = t >= 32 ? 0xffffffffu : (t > 0 ? (1u << t) - 1u : 0u);
+              }
+            } else {
+              const int w = (tb + (j - n_pre) * kBlk) >> 6;
+              const uint64_t a0 = w < p.anc_words ? p.anc[static_cast<int64_t>(gn) * p.anc_words + w] : 0ull;
+              vm[0] = static_cast<uint32_t>(a0);
+              vm[1] = static_cast<uint32_t>(a0 >> 32);
+            }
           }
-        const float mn = fmaxf(m, mloc);
-        const bool grow = mn > m + 8.f;          // also true when m = -inf and mn is finite
-        const float mu = grow ? mn : m;
-        const float msafe = mu == -INFINITY ? 0.f : mu;
-        float rs = 0.f;
-        uint32_t pk[4][16];
+          // raw scores; masked entries become -inf only in partial blocks
+          if (__any_sync(0xffffffffu, (vm[0] & vm[1]) != 0xffffffffu)) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float e0 = ex2(__uint_as_float(xr[q][2 * c]) - msafe);
-            const float e1 = ex2(__uint_as_float(xr[q][2 * c + 1]) - msafe);
-            rs += e0 + e1;
-            pk[q][c] = pack_bf16(e0, e1);
+              for (int c = 0; c < 32; ++c)
+                if (!((vm[q] >> c) & 1u)) xr[q][c] = __float_as_uint(-INFINITY);
           }
-        // P and O are free once PV of the previous block has completed
-        if (j > 0) {
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(xr[q][c]));
+          // running max in base-2 units of scale * q.k (scale > 0, so max commutes)
+          const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+          const float mn = fmaxf(m, mloc);
+          const bool grow = mn > m + 8.f;          // also true when m = -inf and mn is finite
+          const float mu = grow ? mn : m;
+          const float msafe = mu == -INFINITY ? 0.f : mu;
+          float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float e0 = ex2(fmaf(__uint_as_float(xr[q][2 * c]), c2, -msafe));
+              const float e1 = ex2(fmaf(__uint_as_float(xr[q][2 * c + 1]), c2, -msafe));
+              sm4[c & 3] += e0 + e1;
+              pk[q][c] = pack_bf16(e0, e1);
+            }
+          rs = (sm4[0] + sm4[1]) + (sm4[2] + sm4[3]);
+          rescale_row = grow && m != -INFINITY;
+          corr = rescale_row ? ex2(m - mu) : 1.f;
+          m = mu;
+        }
+        // P buffer j&1 is free once PV(j-2) has completed.  O is touched only
+        // when this warp must rescale: then PV(j-1) must have completed too.
+        // Waits go in phase order so a parity wait is never two phases ahead.
+        const bool need_o = warp_live && j > 0 && __any_sync(0xffffffffu, rescale_row);
+        if (j >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(P_FREE + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, err, 11));
+          if (!ok) break;
+        }
+        if (need_o) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar(O_READY), (j - 1) & 1, abort_flag, err, 9));
           if (!ok) break;
-          tc_fence_after();
         }
-        const bool rescale_row = grow && m != -INFINITY;
-        const float corr = rescale_row ? ex2(m - mu) : 1.f;
-        if (__any_sync(0xffffffffu, rescale_row) && j > 0) {
+        tc_fence_after();
+        if (warp_live) {
+          if (need_o) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + 32 * q, o);
-            tmem_ld_wait();
+            for (int q = 0; q < 4; ++q) {
+              uint32_t o[32];
+              tmem_ld32(tO + lane_off + 32 * q, o);
+              tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              pin(o[c]);
-              o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+              for (int c = 0; c < 32; ++c) {
+                pin(o[c]);
+                o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+              }
+              tmem_st32(tO + lane_off + 32 * q, o);
             }
-            tmem_st32(tO + lane_off + 32 * q, o);
+            tmem_st_wait();
           }
-          tmem_st_wait();
-        }
-        l = l * corr + rs;
-        m = mu;
-        // P row -> shared memory, K-major 128-byte swizzle: two 64-key halves
-        uint8_t* prow = sm + kPOff + row * 128;
+          l = l * corr + rs;
+          // P row -> shared memory, K-major 128-byte swizzle (8 chunks of 8 keys)
+          uint8_t* pdst = prow + (j & 1) * kPBytes;
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const int kh = ch >> 3, c8 = ch & 7;
-          uint4 v4 = make_uint4(pk[ch >> 2][(ch & 3) * 4], pk[ch >> 2][(ch & 3) * 4 + 1],
-                                pk[ch >> 2][(ch & 3) * 4 + 2], pk[ch >> 2][(ch & 3) * 4 + 3]);
-          *reinterpret_cast<uint4*>(prow + kh * kHalf + ((c8 ^ (row & 7)) << 4)) = v4;
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint32_t* src = &pk[c8 >> 2][(c8 & 3) * 4];
+            *reinterpret_cast<uint4*>(pdst + ((c8 ^ (row & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
-        mbar_arrive(bar(P_FULL));
+        mbar_arrive(bar(P_FULL + (j & 1)));
       }
-      if (ok) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(O_READY), (nblk - 1) & 1, abort_flag, err, 10));
-        tc_fence_after();
-      }
+      // all PV MMAs complete: the last two P buffers are released in order
+      if (ok && nblk >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(P_FREE + ((nblk - 2) & 1)), ((nblk - 2) >> 1) & 1,
+                                               abort_flag, err, 10));
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(P_FREE + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1,
+                                               abort_flag, err, 10));
+      tc_fence_after();
       // ---- epilogue: O / l
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool write = active && ok;
+      if (warp_live) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_off + 32 * q, o);
-        tmem_ld_wait();
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + 32 * q, o);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pin(o[c]);
-        if (write) {
-          if (p.n_split == 1) {
-            uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(gn) * p.Hq + head) * kD + 32 * q;
+          for (int c = 0; c < 32; ++c) pin(o[c]);
+          if (write) {
+            if (p.n_split == 1) {
+              uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(gn) * p.Hq + head) * kD + 32 * q;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 v4 = make_uint4(pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv),
-                                    pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv),
-                                    pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv),
-                                    pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv));
-              *reinterpret_cast<uint4*>(op + c) = v4;
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v4 = make_uint4(pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv));
+                *reinterpret_cast<uint4*>(op + c) = v4;
+              }
+            } else {
+              const int64_t slot = (static_cast<int64_t>(split) * p.B * p.max_nodes +
+                                    static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
+              float* po = p.ws_o + slot * kD + 32 * q;
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(po + c) =
+                    make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                                __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
             }
-          } else {
-            const int64_t slot = (static_cast<int64_t>(split) * p.B * p.max_nodes +
-                                  static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
-            float* po = p.ws_o + slot * kD + 32 * q;
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              *reinterpret_cast<float4*>(po + c) =
-                  make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                              __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
           }
         }
       }
@@ -500,10 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == L::kMmaWarp) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -540,29 +649,39 @@ bool make_map(CUtensorMap* m, const void* base, int heads, long long tokens, int
 bool attn_tc_supported(int dtype, int d, int Hq, int Hkv) {
   if (dtype != TV_BF16 || d != tc::kD || Hq % Hkv) return false;
   const int g = Hq / Hkv;
-  return g >= 1 && g <= 128 && (128 % g) == 0;
+  return g >= 1 && g <= 64 && (64 % g) == 0;
 }
+
+// 64 live rows when a whole request fits in one 64-row tile, else 128
+static int tc_live(int max_nodes, int g) { return static_cast<long long>(max_nodes) * g <= 64 ? 64 : 128; }
 
 int attn_tc_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm) {
   const int g = Hq / Hkv;
-  const int nq = tc::kRows / g;
+  const int live = tc_live(max_nodes, g);
+  const int nq = live / g;
   const long long tiles = (max_nodes + nq - 1) / nq;
   const long long base = static_cast<long long>(B) * Hkv * tiles;
-  long long s = (2LL * n_sm + base - 1) / base;
+  const long long slots = static_cast<long long>(n_sm) * (live == 64 ? 2 : 1);   // resident CTAs
+  long long s = (2LL * slots + base - 1) / base;
+  if (base >= slots) s = 1;
   s = std::min<long long>(s, std::max(1, (max_prefix + 511) / 512));
   return static_cast<int>(std::max(1LL, std::min(s, 64LL)));
 }
 
-int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st) {
-  static const bool attr_ok = cudaFuncSetAttribute(tc::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(tc::kSmemBytes)) == cudaSuccess;
+template <int LIVE>
+static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long total_prefix, int* err,
+                          cudaStream_t st) {
+  using L = tc::Lay<LIVE>;
+  static const bool attr_ok = cudaFuncSetAttribute(tc::attn_tc_kernel<LIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(L::kSmemBytes)) == cudaSuccess;
   if (!attr_ok) return TV_ECUDA;
   tc::TcParams P;
   std::memset(&P, 0, sizeof(P));
   P.a = p;
   P.err = err;
   const int g = p.Hq / p.Hkv;
-  bool ok = tc::make_map(&P.maps.q, p.q, p.Hq, total_nodes, g, tc::kRows / g) &&
+  const int nq = LIVE / g;
+  bool ok = tc::make_map(&P.maps.q, p.q, p.Hq, total_nodes, g, nq) &&
             tc::make_map(&P.maps.kt, p.k_tree, p.Hkv, total_nodes, 1, tc::kBlk) &&
             tc::make_map(&P.maps.vt, p.v_tree, p.Hkv, total_nodes, 1, tc::kBlk);
   if (ok && total_prefix > 0) {
@@ -573,12 +692,16 @@ int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, 
     P.maps.vp = P.maps.vt;
   }
   if (!ok) return TV_ECUDA;
-  const int nq = tc::kRows / g;
   const int tiles = (p.max_nodes + nq - 1) / nq;
   dim3 grid(p.n_split, tiles, p.B * p.Hkv);
-  tc::attn_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(P);
+  tc::attn_tc_kernel<LIVE><<<grid, L::kThreads, L::kSmemBytes, st>>>(P);
   if (p.n_split > 1) return attn_combine(p, st);
   return launch_status();
+}
+
+int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st) {
+  if (tc_live(p.max_nodes, p.Hq / p.Hkv) == 64) return attn_tc_launch<64>(p, total_nodes, total_prefix, err, st);
+  return attn_tc_launch<128>(p, total_nodes, total_prefix, err, st);
 }
 
 }  // namespace tv

@@ -15,6 +15,8 @@
 //           (deterministic) and writes the outputs.
 #include <float.h>
 
+#include <algorithm>
+
 #include "tv_common.cuh"
 
 namespace tv {
@@ -320,6 +322,287 @@ __global__ void __launch_bounds__(128) vocab_merge_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming variant (used whenever rows and chunk tails are 16-byte aligned).
+//
+// A persistent grid of CTAs walks the (row, chunk) items round-robin.  Each
+// CTA keeps a ring of 8192-element chunks in shared memory, filled by
+// cp.async.bulk copies that thread 0 issues a ring's length ahead, so loads
+// stay in flight while earlier chunks are reduced.  Per chunk: thread maxima;
+// each warp contributes its two largest, 16 distinct elements in all.  The
+// chunk max is the largest; the top-k threshold tau is the k-th largest of
+// the 16, so at least k elements of the chunk are >= tau and every member of
+// its top-k is.  Threads whose own maximum is below tau skip the candidate
+// scan; the others write their candidates straight into the chunk's partial
+// record.  Nothing is ranked per chunk: the per-row merge ranks all
+// candidates, so a chunk costs two barriers and no serial section.
+// ---------------------------------------------------------------------------
+// ring of 8192-element chunks: 4 x 16 KB for bf16, 3 x 32 KB for fp32
+template <typename T> constexpr int stream_stages() { return sizeof(T) == 2 ? 4 : 3; }
+template <typename T> constexpr int stream_chunk_bytes() { return kVChunk * static_cast<int>(sizeof(T)); }
+
+__device__ __forceinline__ uint32_t sm_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (about 2 s); false when it ran out.
+__device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  if (bar_try(bar, parity)) return true;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (bar_try(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 2000000000ull) return false;
+    }
+  }
+  return false;
+}
+
+// 32 values per thread; value t of thread tid is element (t/VEC*256 + tid)*VEC + t%VEC,
+// VEC = elements per 16-byte vector.  With TAIL, entries at or past n_valid
+// become -inf (only the last chunk of a row is partial).
+template <typename T, bool TAIL>
+__device__ __forceinline__ void stage_values(const uint8_t* st, int n_valid, float* v) {
+  constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+#pragma unroll
+  for (int j = 0; j < kVPerThread / VEC; ++j) {
+    const int e0 = (j * kVThreads + threadIdx.x) * VEC;
+    const uint4 w = *reinterpret_cast<const uint4*>(st + e0 * sizeof(T));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[8 * j + 2 * q] = bf16_lo(ws[q]);
+        v[8 * j + 2 * q + 1] = bf16_hi(ws[q]);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[4 * j + q] = __uint_as_float(ws[q]);
+    }
+    if (TAIL) {
+#pragma unroll
+      for (int q = 0; q < VEC; ++q)
+        if (e0 + q >= n_valid) v[VEC * j + q] = -INFINITY;
+    }
+  }
+}
+
+// Partial of one streamed chunk: max, sum of exp(x - max), and every element
+// >= the chunk threshold (up to kSCand of them; ovf = 1 when there were more).
+constexpr int kSCand = 32;
+struct StreamPart {
+  float m, s;
+  int cnt, ovf;
+  int idx[kSCand];
+  float val[kSCand];
+};
+
+__device__ __forceinline__ bool bar_wait_fast(uint32_t bar, uint32_t parity) {
+  return bar_try(bar, parity) || bar_wait(bar, parity);
+}
+
+template <typename T, int KMAX, bool LSE>
+__global__ void __launch_bounds__(kVThreads) vocab_stream_kernel(
+    const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows,
+    int n_chunks, StreamPart* __restrict__ part, int* __restrict__ err) {
+  constexpr int EPT = kVPerThread;                        // 32 values per thread
+  constexpr int VEC = 16 / static_cast<int>(sizeof(T));   // elements per 16 B
+  constexpr int CH = kVChunk;                             // 8192 elements per chunk
+  constexpr int kSStages = stream_stages<T>();
+  constexpr int kSChunkBytes = stream_chunk_bytes<T>();
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[4];
+  __shared__ float s_wmax[kVThreads / 32], s_wtau[kVThreads / 32], s_wsum[kVThreads / 32];
+  __shared__ int s_cnt;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
+  const int G = gridDim.x;
+  if (tid == 0) {
+    for (int s = 0; s < kSStages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_cnt = 0;
+  }
+  __syncthreads();
+  auto issue = [&](int item, int s) {
+    const int row = item / n_chunks, c = item - row * n_chunks;
+    const int src = row_idx ? row_idx[row] : row;
+    const int n = min(CH, V - c * CH);
+    bulk_g2s(sm_u32(ring + s * kSChunkBytes), logits + static_cast<int64_t>(src) * ld + static_cast<int64_t>(c) * CH,
+             static_cast<uint32_t>(n * sizeof(T)), sm_u32(&full[s]));
+  };
+  if (tid == 0)
+    for (int s = 0; s < kSStages; ++s)
+      if (static_cast<int>(blockIdx.x) + s * G < items) issue(blockIdx.x + s * G, s);
+
+  int it = 0;
+  for (int item = blockIdx.x; item < items; item += G, ++it) {
+    const int s = it % kSStages;
+    const int c = item % n_chunks;
+    const int base = c * CH;
+    const int n_valid = min(CH, V - base);
+    const bool ok = bar_wait_fast(sm_u32(&full[s]), (it / kSStages) & 1);
+    float v[EPT];
+    if (ok && n_valid == CH) stage_values<T, false>(ring + s * kSChunkBytes, CH, v);
+    else stage_values<T, true>(ring + s * kSChunkBytes, ok ? n_valid : 0, v);
+
+    float mx = v[0];
+#pragma unroll
+    for (int t = 1; t < EPT; ++t) mx = fmaxf(mx, v[t]);
+    const float my_max = mx;
+    // the two largest thread maxima of the warp: 16 distinct elements per chunk
+    const float wm = warp_max(mx);
+    const unsigned hit = __ballot_sync(0xffffffffu, my_max == wm);
+    const float w2 = warp_max(lane == __ffs(hit) - 1 ? -INFINITY : my_max);
+    if (lane == 0) { s_wmax[warp] = wm; s_wtau[warp] = w2; }
+    const bool all_ok = __syncthreads_and(ok) != 0;       // block-uniform outcome of the wait
+    float M = s_wmax[0];
+#pragma unroll
+    for (int w = 1; w < kVThreads / 32; ++w) M = fmaxf(M, s_wmax[w]);
+    // tau = KMAX-th largest of those 16 values (ties by slot): at least KMAX
+    // elements of the chunk are >= tau, so its top-KMAX all are.
+    float tau = M;
+    if (KMAX > 1) {
+      const float u = lane < 8 ? s_wmax[lane] : (lane < 16 ? s_wtau[lane - 8] : -INFINITY);
+      int rank = 0;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float um = __shfl_sync(0xffffffffu, u, m);
+        rank += (um > u) || (um == u && m < lane);
+      }
+      const unsigned sel = __ballot_sync(0xffffffffu, lane < 16 && rank == KMAX - 1);
+      tau = __shfl_sync(0xffffffffu, u, __ffs(sel) - 1);
+    }
+    if (LSE) {
+      const float mb = M * kLog2e;
+      float sum = 0.f;
+#pragma unroll
+      for (int t = 0; t < EPT; ++t) sum += ex2(fmaf(v[t], kLog2e, -mb));
+      sum = warp_sum(sum);
+      if (lane == 0) s_wsum[warp] = sum;
+    }
+    StreamPart* out = part + item;
+    if (my_max >= tau) {
+#pragma unroll
+      for (int t = 0; t < EPT; ++t) {
+        if (v[t] >= tau) {
+          const int pos = atomicAdd(&s_cnt, 1);
+          if (pos < kSCand) {
+            out->val[pos] = v[t];
+            out->idx[pos] = base + ((t / VEC) * kVThreads + tid) * VEC + (t % VEC);
+          }
+        }
+      }
+    }
+    __syncthreads();   // stage s consumed; candidate count final
+    if (tid == 0) {
+      const int cnt = s_cnt;
+      s_cnt = 0;
+      float sum = 0.f;
+      if (LSE) {
+#pragma unroll
+        for (int w = 0; w < kVThreads / 32; ++w) sum += s_wsum[w];
+      }
+      out->m = M;
+      out->s = sum;
+      out->cnt = min(cnt, kSCand);
+      out->ovf = cnt > kSCand;
+      if (all_ok && item + kSStages * G < items) issue(item + kSStages * G, s);
+    }
+    if (!all_ok) {
+      if (tid == 0 && err) *err = 1;
+      break;
+    }
+  }
+}
+
+// One warp per row: chunk maxima and sums, then every chunk's candidates go
+// into per-lane top-k lists (a chunk that overflowed its candidate list is
+// rescanned here, all of it), and a warp merge yields the row's top-k.
+template <typename T, int KMAX, bool LSE>
+__global__ void __launch_bounds__(128) vocab_stream_merge_kernel(
+    const StreamPart* __restrict__ part, int n_chunks, int rows, const T* __restrict__ logits, int V,
+    int64_t ld, const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_val, float* __restrict__ row_max,
+    float* __restrict__ row_lse) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int src = row_idx ? row_idx[row] : row;
+  const StreamPart* p = part + static_cast<int64_t>(row) * n_chunks;
+  float M = -INFINITY;
+  for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, p[c].m);
+  M = warp_max(M);
+  float S = 0.f;
+  if (LSE) {
+    for (int c = lane; c < n_chunks; c += 32) S += p[c].s * ex2((p[c].m - M) * kLog2e);
+    S = warp_sum(S);
+  }
+  float lv[KMAX];
+  int li[KMAX];
+#pragma unroll
+  for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
+  const T* x = logits + static_cast<int64_t>(src) * ld;
+  for (int c = 0; c < n_chunks; ++c) {
+    if (!p[c].ovf) {
+      if (lane < p[c].cnt) list_insert<KMAX>(lv, li, p[c].val[lane], p[c].idx[lane]);
+    } else {
+      const int e1 = min(V, (c + 1) * kVChunk);
+      for (int e = c * kVChunk + lane; e < e1; e += 32) {
+        float xv;
+        if constexpr (sizeof(T) == 2) xv = bf16_at(reinterpret_cast<const uint16_t*>(x) + e);
+        else xv = reinterpret_cast<const float*>(x)[e];
+        list_insert<KMAX>(lv, li, xv, e);
+      }
+    }
+  }
+  float ov[KMAX];
+  int oi[KMAX];
+  warp_merge_lists<KMAX>(lv, li, ov, oi);
+  const int dst = src;
+  if (lane == 0) {
+    argmax[dst] = oi[0];
+    if (row_max) row_max[dst] = M;
+    if (LSE && row_lse) row_lse[dst] = M + logf(S);
+  }
+  if (k > 0 && lane < k) {
+    float val = ov[0];
+    int idx = oi[0];
+#pragma unroll
+    for (int q = 1; q < KMAX; ++q)
+      if (lane == q) { val = ov[q]; idx = oi[q]; }
+    if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = idx;
+    if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = val;
+  }
+}
+
+int sm_count_cached() {
+  static const int n = [] {
+    int dev = 0, c = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) return 148;
+    return c;
+  }();
+  return n;
+}
+
 template <typename T, int KMAX, bool LSE>
 int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* row_idx, int k,
                  int32_t* argmax, int32_t* topk_idx, float* topk_val, float* row_max,
@@ -327,6 +610,25 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
   const int n_chunks = (V + kVChunk - 1) / kVChunk;
   const bool vec_ok = aligned(logits, 16) && ((ld * static_cast<int64_t>(sizeof(T))) % 16 == 0);
   auto* part = reinterpret_cast<VocabPart<KMAX>*>(ws);
+  // the streaming kernel's bulk copies need 16-byte rows and chunk tails
+  const bool stream_ok = vec_ok && (static_cast<int64_t>(V) * sizeof(T)) % 16 == 0;
+  if (stream_ok) {
+    constexpr int smem = stream_stages<T>() * stream_chunk_bytes<T>();
+    static const bool attr = cudaFuncSetAttribute(vocab_stream_kernel<T, KMAX, LSE>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  smem) == cudaSuccess;
+    if (!attr) return TV_ECUDA;
+    const int items = rows * n_chunks;
+    const int per_sm = sizeof(T) == 2 ? 3 : 2;
+    const int grid = std::min(items, per_sm * sm_count_cached());
+    auto* sp = reinterpret_cast<StreamPart*>(ws);
+    vocab_stream_kernel<T, KMAX, LSE><<<grid, kVThreads, smem, st>>>(logits, V, ld, row_idx, rows, n_chunks,
+                                                                      sp, nullptr);
+    const int wpb = 4;
+    vocab_stream_merge_kernel<T, KMAX, LSE><<<(rows + wpb - 1) / wpb, 32 * wpb, 0, st>>>(
+        sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax, topk_idx, topk_val, row_max, row_lse);
+    return launch_status();
+  }
   dim3 g1(n_chunks, rows);
   vocab_partial_kernel<T, KMAX, LSE><<<g1, kVThreads, 0, st>>>(logits, V, ld, row_idx, vec_ok, part);
   const int wpb = 4;
@@ -357,7 +659,7 @@ TV_API size_t vocab_argmax_topk_workspace_size(int rows, int V, int k) {
   if (rows <= 0 || V <= 0) return 0;
   const size_t n_chunks = (static_cast<size_t>(V) + tv::kVChunk - 1) / tv::kVChunk;
   const size_t kmax = k <= 1 ? 1 : (k <= 8 ? 8 : 16);
-  const size_t part = 2 * sizeof(float) + kmax * (sizeof(float) + sizeof(int));
+  const size_t part = std::max(2 * sizeof(float) + kmax * (sizeof(float) + sizeof(int)), sizeof(tv::StreamPart));
   return static_cast<size_t>(rows) * n_chunks * part;
 }
 
