@@ -1,17 +1,21 @@
 // dcut_select: D-cut prefix-product scores and batch-global budget selection
 // (D-cut page, technical summary §2 core mechanism and pipeline; §1 B x (D+1)).
 //
-// One CTA of 1024 threads, everything in shared memory (T = B(D+1) <= 8192):
+// One CTA of 1024 threads (T = B(D+1) <= 8192):
 //   1. one thread per request forms s[r,j] = s[r,j-1] * conf[r,j-1] strictly
 //      left to right in fp32 (products only, so nothing can be contracted);
-//   2. the T positions are sorted by the 64-bit key (~bits(s), t): scores are
+//   2. the positions are sorted by the 64-bit key (~bits(s), t): scores are
 //      non-negative, so their IEEE bits order like the values, and the key
 //      order is (s desc, position asc) = (s desc, r asc, j asc).  A bitonic
-//      network over the next power of two (padding keys sort last);
+//      network over n = 1024 E keys (E per thread, padding keys sort last):
+//      compare distances below E stay in a thread, distances below 32 E are
+//      warp shuffles, only the larger ones go through shared memory (15 of
+//      the 55 stages for T <= 1024, one barrier each);
 //   3. rank(t) = sorted position; t is kept for budget K iff rank(t) < K;
-//   4. one block-wide exclusive scan of the keep flags per budget gives the
-//      packed slot of every kept position, the per-request offsets and lengths
-//      (no assumption that the kept set is a prefix).
+//   4. one block-wide exclusive scan of the keep counts of every budget at
+//      once (two budgets per 32-bit word) gives the packed slot of every kept
+//      position and the per-request offsets; one warp per request counts the
+//      lengths (no assumption that the kept set is a prefix).
 #include <cmath>
 
 #include "tv_common.cuh"
@@ -24,109 +28,189 @@ constexpr int kDcutThreads = 1024;
 
 struct DcutK { int K[kDcutMaxRho]; };
 
-// exclusive scan of one int per thread across the 1024-thread block
-__device__ __forceinline__ int block_excl_scan(int x, int* s_w, int* total) {
+// Exclusive scan of four words per thread across the 1024-thread block, each
+// word holding two 16-bit counts (totals stay below 2^16: T <= 8192).
+__device__ __forceinline__ uint4 block_excl_scan4(uint4 x, uint4* s_w, uint4* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int v = x;
+  uint4 v = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
+    uint4 y;
+    y.x = __shfl_up_sync(0xffffffffu, v.x, o);
+    y.y = __shfl_up_sync(0xffffffffu, v.y, o);
+    y.z = __shfl_up_sync(0xffffffffu, v.z, o);
+    y.w = __shfl_up_sync(0xffffffffu, v.w, o);
+    if (lane >= o) { v.x += y.x; v.y += y.y; v.z += y.z; v.w += y.w; }
   }
   if (lane == 31) s_w[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int w = s_w[lane];
-    int iw = w;
+    const uint4 w = s_w[lane];
+    uint4 iw = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, iw, o);
-      if (lane >= o) iw += y;
+      uint4 y;
+      y.x = __shfl_up_sync(0xffffffffu, iw.x, o);
+      y.y = __shfl_up_sync(0xffffffffu, iw.y, o);
+      y.z = __shfl_up_sync(0xffffffffu, iw.z, o);
+      y.w = __shfl_up_sync(0xffffffffu, iw.w, o);
+      if (lane >= o) { iw.x += y.x; iw.y += y.y; iw.z += y.z; iw.w += y.w; }
     }
-    s_w[lane] = iw - w;                 // exclusive warp offsets
-    if (lane == 31) s_w[32] = iw;       // block total
+    s_w[lane] = make_uint4(iw.x - w.x, iw.y - w.y, iw.z - w.z, iw.w - w.w);   // exclusive
+    if (lane == 31) s_w[32] = iw;                                              // block total
   }
   __syncthreads();
-  const int r = s_w[warp] + v - x;
+  const uint4 base = s_w[warp];
   *total = s_w[32];
-  __syncthreads();                      // s_w reusable
-  return r;
+  return make_uint4(base.x + v.x - x.x, base.y + v.y - x.y, base.z + v.z - x.z, base.w + v.w - x.w);
 }
 
-__global__ void __launch_bounds__(kDcutThreads) dcut_kernel(
+__device__ __forceinline__ int half16(const uint4& w, int a) {
+  const uint32_t word = (a >> 1) == 0 ? w.x : (a >> 1) == 1 ? w.y : (a >> 1) == 2 ? w.z : w.w;
+  return static_cast<int>((a & 1) ? (word >> 16) : (word & 0xffffu));
+}
+
+// E keys per thread; element i = tid * E + e of the n = 1024 E sorted keys.
+template <int E>
+__global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
     const float* __restrict__ conf, int B, int D, int n_rho, DcutK ks, float* __restrict__ score,
     uint8_t* __restrict__ keep, int32_t* __restrict__ keep_len, int32_t* __restrict__ pack_off,
     int32_t* __restrict__ pack_idx) {
-  extern __shared__ unsigned long long s_key[];                       // [Tp] sort keys
+  constexpr int n = kDcutThreads * E;
+  extern __shared__ unsigned long long s_key[];                       // [n] sort keys
   int* s_rank = reinterpret_cast<int*>(s_key + kDcutMaxPos);          // [T]
-  __shared__ int s_w[33];
-  const int tid = threadIdx.x;
+  __shared__ uint4 s_w[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = D + 1;
   const int T = B * N;
-  int Tp = 1;
-  while (Tp < T) Tp <<= 1;
 
-  // 1. scores, and their sort keys
-  for (int r = tid; r < B; r += blockDim.x) {
+  // 1. confidences into shared memory with one coalesced pass (they sit in
+  //    the rank array's space, which is not needed until step 3)
+  float* s_conf = reinterpret_cast<float*>(s_rank);
+  for (int i = tid; i < B * D; i += kDcutThreads) s_conf[i] = conf[i];
+  __syncthreads();
+  for (int r = tid; r < B; r += kDcutThreads) {
     float s = 1.f;
     for (int j = 0; j <= D; ++j) {
-      if (j > 0) s = __fmul_rn(s, conf[static_cast<int64_t>(r) * D + j - 1]);
+      if (j > 0) s = __fmul_rn(s, s_conf[r * D + j - 1]);
       const int t = r * N + j;
-      score[t] = s;
       s_key[t] = (static_cast<unsigned long long>(~__float_as_uint(s)) << 32) | static_cast<unsigned>(t);
     }
   }
-  for (int t = T + tid; t < Tp; t += blockDim.x) s_key[t] = ~0ull;
+  for (int t = T + tid; t < n; t += kDcutThreads) s_key[t] = ~0ull;
   __syncthreads();
+  // scores out, coalesced (the key's high word holds the score's bits)
+  for (int t = tid; t < T; t += kDcutThreads) score[t] = __uint_as_float(~static_cast<unsigned>(s_key[t] >> 32));
+  unsigned long long key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) key[e] = s_key[tid * E + e];
+  __syncthreads();   // keys read before the network writes them back
 
-  // 2. bitonic sort, ascending keys
-  for (int k = 2; k <= Tp; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < Tp; i += blockDim.x) {
-        const int p = i ^ j;
-        if (p > i) {
-          const unsigned long long a = s_key[i], b = s_key[p];
-          const bool up = (i & k) == 0;
-          if ((a > b) == up) { s_key[i] = b; s_key[p] = a; }
+  // 2. bitonic network, ascending keys
+  for (int k = 2; k <= n; k <<= 1) {
+    int j = k >> 1;
+    if (j >= 32 * E) {   // cross-warp distances through shared memory
+#pragma unroll
+      for (int e = 0; e < E; ++e) s_key[tid * E + e] = key[e];
+      __syncthreads();
+      for (; j >= 32 * E; j >>= 1) {
+#pragma unroll
+        for (int q = 0; q < E; ++q) {
+          const int i = q * kDcutThreads + tid;
+          const int p = i ^ j;
+          if (p > i) {
+            const unsigned long long a = s_key[i], b = s_key[p];
+            if ((a > b) == ((i & k) == 0)) { s_key[i] = b; s_key[p] = a; }
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) key[e] = s_key[tid * E + e];
+    }
+    for (; j >= E; j >>= 1) {   // partner in lane ^ (j / E), same slot
+      const int m = j / E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key[e], m);
+        const int i = tid * E + e;
+        const bool take_min = ((i & j) == 0) == ((i & k) == 0);
+        key[e] = take_min ? (o < key[e] ? o : key[e]) : (o > key[e] ? o : key[e]);
+      }
+    }
+#pragma unroll
+    for (int jj = E >> 1; jj >= 1; jj >>= 1) {   // partner in the same thread
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if ((e & jj) == 0) {
+          const int i = tid * E + e;
+          const unsigned long long a = key[e], b = key[e | jj];
+          if ((a > b) == ((i & k) == 0)) { key[e] = b; key[e | jj] = a; }
         }
       }
-      __syncthreads();
     }
   }
-  // 3. rank of each position
-  for (int i = tid; i < T; i += blockDim.x) s_rank[static_cast<int>(s_key[i] & 0xffffffffu)] = i;
+  // 3. rank of each position (padding keys carry t = 0xffffffff)
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const unsigned t = static_cast<unsigned>(key[e] & 0xffffffffu);
+    if (t < static_cast<unsigned>(T)) s_rank[t] = tid * E + e;
+  }
   __syncthreads();
 
-  // 4. per budget: flags, exclusive scan, packing
-  const int per = (T + blockDim.x - 1) / blockDim.x;     // consecutive positions per thread
+  // 4. flags and counts of every budget, one scan for all of them
+  const int per = (T + kDcutThreads - 1) / kDcutThreads;   // consecutive positions per thread (<= E)
   const int t0 = tid * per;
-  for (int a = 0; a < n_rho; ++a) {
+  int rk[E];
+  uint32_t cw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int q = 0; q < E; ++q) {
+    const int t = t0 + q;
+    rk[q] = (q < per && t < T) ? s_rank[t] : INT32_MAX;
+#pragma unroll
+    for (int a = 0; a < kDcutMaxRho; ++a)
+      if (a < n_rho && rk[q] < ks.K[a]) cw[a >> 1] += (a & 1) ? 0x10000u : 1u;
+  }
+  uint4 total;
+  const uint4 ex = block_excl_scan4(make_uint4(cw[0], cw[1], cw[2], cw[3]), s_w, &total);
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) {
+    if (a >= n_rho) break;
     const int K = ks.K[a];
+    const int tot = half16(total, a);
+    int o = half16(ex, a);
     uint8_t* kp = keep + static_cast<int64_t>(a) * T;
-    int mine = 0;
-    for (int t = t0; t < min(T, t0 + per); ++t) {
-      const int f = s_rank[t] < K;
-      kp[t] = static_cast<uint8_t>(f);
-      mine += f;
-    }
-    int total = 0;
-    int o = block_excl_scan(mine, s_w, &total);
     int32_t* pi = pack_idx ? pack_idx + static_cast<int64_t>(a) * T : nullptr;
-    for (int t = t0; t < min(T, t0 + per); ++t) {
-      const int f = s_rank[t] < K;
-      const int r = t / N, j = t - r * N;
-      if (j == 0 && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + r] = o;   // kept before request r
-      if (f && pi) pi[o] = t;
-      o += f;
+#pragma unroll
+    for (int q = 0; q < E; ++q) {
+      const int t = t0 + q;
+      if (q < per && t < T) {
+        const int f = rk[q] < K;
+        kp[t] = static_cast<uint8_t>(f);
+        const int r = t / N;
+        if (t == r * N && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + r] = o;   // kept before request r
+        if (f && pi) pi[o] = t;
+        o += f;
+      }
     }
-    if (tid == 0 && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + B] = total;
+    if (tid == 0 && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + B] = tot;
     if (pi)
-      for (int q = total + tid; q < T; q += blockDim.x) pi[q] = -1;
-    // keep_len[r] = kept positions of request r
-    for (int r = tid; r < B; r += blockDim.x) {
-      int c = 0;
-      for (int j = 0; j < N; ++j) c += s_rank[r * N + j] < K;
-      keep_len[static_cast<int64_t>(a) * B + r] = c;
+      for (int q = tot + tid; q < T; q += kDcutThreads) pi[q] = -1;
+  }
+  // keep_len[r]: one warp per request, lanes over its positions
+  for (int r = warp; r < B; r += kDcutThreads / 32) {
+    int c[kDcutMaxRho] = {};
+    for (int j = lane; j < N; j += 32) {
+      const int x = s_rank[r * N + j];
+#pragma unroll
+      for (int a = 0; a < kDcutMaxRho; ++a) c[a] += a < n_rho && x < ks.K[a];
+    }
+#pragma unroll
+    for (int a = 0; a < kDcutMaxRho; ++a) {
+      if (a < n_rho) {
+        const int sum = __reduce_add_sync(0xffffffffu, c[a]);
+        if (lane == 0) keep_len[static_cast<int64_t>(a) * B + r] = sum;
+      }
     }
   }
 }
@@ -155,12 +239,21 @@ TV_API int dcut_select(const float* conf, int B, int D, const float* rho, int n_
     if (!(r >= 0.0 && r <= 1.0)) return TV_EINVAL;
     ks.K[a] = static_cast<int>(std::floor(r * static_cast<double>(T) + 0.5));
   }
-  static const int smem = [] {
-    const int bytes = tv::kDcutMaxPos * static_cast<int>(sizeof(unsigned long long) + sizeof(int));
-    cudaFuncSetAttribute(tv::dcut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    return bytes;
+  const int bytes = tv::kDcutMaxPos * static_cast<int>(sizeof(unsigned long long) + sizeof(int));
+  static const bool attr = [bytes] {
+    bool ok = true;
+    ok &= cudaFuncSetAttribute(tv::dcut_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tv::dcut_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tv::dcut_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tv::dcut_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    return ok;
   }();
-  tv::dcut_kernel<<<1, tv::kDcutThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
+  if (!attr) return TV_ECUDA;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  const int Ti = static_cast<int>(T);
+  if (Ti <= 1024) tv::dcut_kernel<1><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
+  else if (Ti <= 2048) tv::dcut_kernel<2><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
+  else if (Ti <= 4096) tv::dcut_kernel<4><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
+  else tv::dcut_kernel<8><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
   return tv::launch_status();
 }

@@ -13,6 +13,7 @@
 //           Only elements >= tau (typically a dozen) are ranked.
 //   pass 2  one warp per row merges the chunk partials in chunk order
 //           (deterministic) and writes the outputs.
+#include <cuda_bf16.h>
 #include <float.h>
 
 #include <algorithm>
@@ -328,14 +329,14 @@ __global__ void __launch_bounds__(128) vocab_merge_kernel(
 // A persistent grid of CTAs walks the (row, chunk) items round-robin.  Each
 // CTA keeps a ring of 8192-element chunks in shared memory, filled by
 // cp.async.bulk copies that thread 0 issues a ring's length ahead, so loads
-// stay in flight while earlier chunks are reduced.  Per chunk: thread maxima;
-// each warp contributes its two largest, 16 distinct elements in all.  The
-// chunk max is the largest; the top-k threshold tau is the k-th largest of
-// the 16, so at least k elements of the chunk are >= tau and every member of
-// its top-k is.  Threads whose own maximum is below tau skip the candidate
+// stay in flight while earlier chunks are reduced.  Per chunk: thread maxima
+// (bf16 pairs at a time), then each warp's top few thread maxima; the chunk
+// max is the largest of those and the top-k threshold tau their k-th largest,
+// so at least k distinct elements are >= tau and every member of the chunk's
+// top-k is.  Threads whose own maximum is below tau skip the candidate
 // scan; the others write their candidates straight into the chunk's partial
 // record.  Nothing is ranked per chunk: the per-row merge ranks all
-// candidates, so a chunk costs two barriers and no serial section.
+// candidates, so a chunk costs one block barrier and no serial section.
 // ---------------------------------------------------------------------------
 // ring of 8192-element chunks: 4 x 16 KB for bf16, 3 x 32 KB for fp32
 template <typename T> constexpr int stream_stages() { return sizeof(T) == 2 ? 4 : 3; }
@@ -417,19 +418,51 @@ __device__ __forceinline__ bool bar_wait_fast(uint32_t bar, uint32_t parity) {
   return bar_try(bar, parity) || bar_wait(bar, parity);
 }
 
+// Warp-wide float maximum in one instruction (sm_100 family).
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// k-th largest (k >= 1) of one value per lane: k - 1 rounds that drop the
+// first lane holding the current maximum.
+__device__ __forceinline__ float warp_kth_largest(float v, int k) {
+  for (int r = 1; r < k; ++r) {
+    const float m = redux_max(v);
+    const unsigned hit = __ballot_sync(0xffffffffu, v == m);
+    if (static_cast<int>(threadIdx.x & 31) == __ffs(hit) - 1) v = -INFINITY;
+  }
+  return redux_max(v);
+}
+
+// Thread maxima each warp contributes to the chunk threshold: the largest P of
+// its 32 (distinct threads), so the KMAX-th largest of the 8 * P collected
+// values has at least KMAX distinct chunk elements at or above it.  P = 2 for
+// k <= 8 and 4 for k <= 16 keep the expected number of candidates per chunk
+// near k (about 9 for k = 8 on Gaussian logits) and far below kSCand.
+template <int KMAX> constexpr int tau_per_warp() { return KMAX == 1 ? 1 : (KMAX <= 8 ? 2 : 4); }
+
 template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(kVThreads) vocab_stream_kernel(
+__global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
     const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows,
     int n_chunks, StreamPart* __restrict__ part, int* __restrict__ err) {
   constexpr int EPT = kVPerThread;                        // 32 values per thread
   constexpr int VEC = 16 / static_cast<int>(sizeof(T));   // elements per 16 B
   constexpr int CH = kVChunk;                             // 8192 elements per chunk
+  constexpr int NW = kVThreads / 32;
+  constexpr int P = tau_per_warp<KMAX>();
+  static_assert(NW * P <= 32, "threshold values must fit one warp");
   constexpr int kSStages = stream_stages<T>();
   constexpr int kSChunkBytes = stream_chunk_bytes<T>();
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[4];
-  __shared__ float s_wmax[kVThreads / 32], s_wtau[kVThreads / 32], s_wsum[kVThreads / 32];
-  __shared__ int s_cnt;
+  // double-buffered by item parity: item i writes buffer i & 1 before the
+  // block barrier of item i and it is read after it, so one barrier per item
+  // suffices
+  __shared__ float s_top[2][NW * P];
+  __shared__ float s_wsum[2][NW];
+  __shared__ int s_cnt[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(kVThreads) vocab_stream_kernel(
     for (int s = 0; s < kSStages; ++s)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    s_cnt = 0;
+    s_cnt[0] = s_cnt[1] = 0;
   }
   __syncthreads();
   auto issue = [&](int item, int s) {
@@ -452,136 +485,308 @@ __global__ void __launch_bounds__(kVThreads) vocab_stream_kernel(
     for (int s = 0; s < kSStages; ++s)
       if (static_cast<int>(blockIdx.x) + s * G < items) issue(blockIdx.x + s * G, s);
 
+  // thread 0 closes an item's record one item later, once all its candidates are in
+  float rec_m = 0.f, rec_s = 0.f;
+  auto close_record = [&](int item, int buf) {
+    StreamPart* o = part + item;
+    const int cnt = s_cnt[buf];
+    s_cnt[buf] = 0;
+    o->m = rec_m;
+    o->s = rec_s;
+    o->cnt = min(cnt, kSCand);
+    o->ovf = cnt > kSCand;
+  };
+
+  const int dc = G % n_chunks;                // chunk index advances by G mod n_chunks
+  int c = blockIdx.x % n_chunks;
   int it = 0;
+  bool all_ok = true;
   for (int item = blockIdx.x; item < items; item += G, ++it) {
-    const int s = it % kSStages;
-    const int c = item % n_chunks;
+    const int s = it % kSStages, b = it & 1;
     const int base = c * CH;
     const int n_valid = min(CH, V - base);
     const bool ok = bar_wait_fast(sm_u32(&full[s]), (it / kSStages) & 1);
+    const uint8_t* st = ring + s * kSChunkBytes;
+    // bf16 without exponentials on a full chunk: keep the packed pairs and
+    // take the maximum two at a time; otherwise unpack to fp32
+    const bool packed = sizeof(T) == 2 && !LSE && ok && n_valid == CH;
     float v[EPT];
-    if (ok && n_valid == CH) stage_values<T, false>(ring + s * kSChunkBytes, CH, v);
-    else stage_values<T, true>(ring + s * kSChunkBytes, ok ? n_valid : 0, v);
-
-    float mx = v[0];
+    uint32_t raw[EPT / 2];
+    float my_max;
+    if (packed) {
+      __nv_bfloat162 pm = __float2bfloat162_rn(-INFINITY);
 #pragma unroll
-    for (int t = 1; t < EPT; ++t) mx = fmaxf(mx, v[t]);
-    const float my_max = mx;
-    // the two largest thread maxima of the warp: 16 distinct elements per chunk
-    const float wm = warp_max(mx);
-    const unsigned hit = __ballot_sync(0xffffffffu, my_max == wm);
-    const float w2 = warp_max(lane == __ffs(hit) - 1 ? -INFINITY : my_max);
-    if (lane == 0) { s_wmax[warp] = wm; s_wtau[warp] = w2; }
-    const bool all_ok = __syncthreads_and(ok) != 0;       // block-uniform outcome of the wait
-    float M = s_wmax[0];
-#pragma unroll
-    for (int w = 1; w < kVThreads / 32; ++w) M = fmaxf(M, s_wmax[w]);
-    // tau = KMAX-th largest of those 16 values (ties by slot): at least KMAX
-    // elements of the chunk are >= tau, so its top-KMAX all are.
-    float tau = M;
-    if (KMAX > 1) {
-      const float u = lane < 8 ? s_wmax[lane] : (lane < 16 ? s_wtau[lane - 8] : -INFINITY);
-      int rank = 0;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float um = __shfl_sync(0xffffffffu, u, m);
-        rank += (um > u) || (um == u && m < lane);
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
+        raw[4 * j] = w.x; raw[4 * j + 1] = w.y; raw[4 * j + 2] = w.z; raw[4 * j + 3] = w.w;
       }
-      const unsigned sel = __ballot_sync(0xffffffffu, lane < 16 && rank == KMAX - 1);
-      tau = __shfl_sync(0xffffffffu, u, __ffs(sel) - 1);
-    }
-    if (LSE) {
-      const float mb = M * kLog2e;
-      float sum = 0.f;
 #pragma unroll
-      for (int t = 0; t < EPT; ++t) sum += ex2(fmaf(v[t], kLog2e, -mb));
+      for (int q = 0; q < EPT / 2; ++q) pm = __hmax2(pm, *reinterpret_cast<const __nv_bfloat162*>(&raw[q]));
+      my_max = fmaxf(__low2float(pm), __high2float(pm));
+    } else {
+      if (ok && n_valid == CH) stage_values<T, false>(st, CH, v);
+      else stage_values<T, true>(st, ok ? n_valid : 0, v);
+      my_max = v[0];
+#pragma unroll
+      for (int t = 1; t < EPT; ++t) my_max = fmaxf(my_max, v[t]);
+    }
+    // per-warp top-P thread maxima
+    const float wmax = redux_max(my_max);
+    if (lane == 0) s_top[b][warp * P] = wmax;
+    if constexpr (P > 1) {
+      float mine = my_max, top = wmax;
+#pragma unroll
+      for (int p = 1; p < P; ++p) {
+        const unsigned hit = __ballot_sync(0xffffffffu, mine == top);
+        if (lane == __ffs(hit) - 1) mine = -INFINITY;
+        top = redux_max(mine);
+        if (lane == 0) s_top[b][warp * P + p] = top;
+      }
+    }
+    if constexpr (LSE) {   // sum of exp(x - warp max)
+      float sum = 0.f;
+      if (wmax != -INFINITY) {
+        const float mb = wmax * kLog2e;
+#pragma unroll
+        for (int t = 0; t < EPT; ++t) sum += ex2(fmaf(v[t], kLog2e, -mb));
+      }
       sum = warp_sum(sum);
-      if (lane == 0) s_wsum[warp] = sum;
+      if (lane == 0) s_wsum[b][warp] = sum;
     }
-    StreamPart* out = part + item;
-    if (my_max >= tau) {
-#pragma unroll
-      for (int t = 0; t < EPT; ++t) {
-        if (v[t] >= tau) {
-          const int pos = atomicAdd(&s_cnt, 1);
-          if (pos < kSCand) {
-            out->val[pos] = v[t];
-            out->idx[pos] = base + ((t / VEC) * kVThreads + tid) * VEC + (t % VEC);
-          }
-        }
-      }
-    }
-    __syncthreads();   // stage s consumed; candidate count final
+    all_ok = __syncthreads_and(ok) != 0;   // block-uniform outcome of the wait
+    // every read of ring slot s happened before the barrier: refill it now
     if (tid == 0) {
-      const int cnt = s_cnt;
-      s_cnt = 0;
-      float sum = 0.f;
-      if (LSE) {
-#pragma unroll
-        for (int w = 0; w < kVThreads / 32; ++w) sum += s_wsum[w];
-      }
-      out->m = M;
-      out->s = sum;
-      out->cnt = min(cnt, kSCand);
-      out->ovf = cnt > kSCand;
+      if (it > 0) close_record(item - G, b ^ 1);
       if (all_ok && item + kSStages * G < items) issue(item + kSStages * G, s);
     }
-    if (!all_ok) {
-      if (tid == 0 && err) *err = 1;
-      break;
+    if (!all_ok) break;
+    const float tv = lane < NW * P ? s_top[b][lane] : -INFINITY;
+    const float M = redux_max(tv);
+    const float tau = KMAX == 1 ? M : warp_kth_largest(tv, KMAX);
+    if (tid == 0) {
+      float ssum = 0.f;
+      if constexpr (LSE) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float wm = s_top[b][w * P];
+          if (wm != -INFINITY) ssum += s_wsum[b][w] * ex2((wm - M) * kLog2e);
+        }
+      }
+      rec_m = M;
+      rec_s = ssum;
+    }
+    if (my_max >= tau) {
+      StreamPart* out = part + item;
+      auto put = [&](float val, int e) {
+        const int pos = atomicAdd(&s_cnt[b], 1);
+        if (pos < kSCand) {
+          out->val[pos] = val;
+          out->idx[pos] = base + e;
+        }
+      };
+      if (packed) {
+        // tau is one of the chunk's elements, so exact in bf16
+        const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
+#pragma unroll
+        for (int q = 0; q < EPT / 2; ++q) {
+          const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&raw[q]), t2);
+          if (msk) {
+            const int e = ((q / 4) * kVThreads + tid) * VEC + 2 * (q % 4);
+            if (msk & 0xffffu) put(bf16_lo(raw[q]), e);
+            if (msk >> 16) put(bf16_hi(raw[q]), e + 1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < EPT; ++t)
+          if (v[t] >= tau) put(v[t], ((t / VEC) * kVThreads + tid) * VEC + (t % VEC));
+      }
+    }
+    c += dc;
+    if (c >= n_chunks) c -= n_chunks;
+  }
+  if (!all_ok) {
+    if (tid == 0 && err) *err = 1;
+    return;
+  }
+  __syncthreads();
+  if (tid == 0 && it > 0) close_record(blockIdx.x + (it - 1) * G, (it - 1) & 1);
+}
+
+// One warp per row.  The warp reads the row's chunk headers (max, sum,
+// candidate count, overflow) with one 16-byte load per lane and takes the
+// row max and sum.  Row threshold: the KMAX-th largest chunk maximum; KMAX
+// distinct elements reach it, so every member of the row's top-k is >= it,
+// and only chunks whose maximum reaches it (about KMAX of them) are opened.
+// Their candidates >= the threshold (a chunk that overflowed is rescanned
+// from the logits) are compacted into a shared buffer, usually a dozen
+// entries, which a 32-lane bitonic sort orders.  Rows with more than 32
+// buffered candidates use per-lane lists; rows with more than the buffer
+// holds (heavy ties) or more than 32 chunks take the plain path over every
+// record.
+constexpr int kMergeWarps = 4;
+constexpr int kMergeBuf = 128;
+
+// Sort one (value, index) pair per lane by (value desc, index asc): lane 0 best.
+__device__ __forceinline__ void warp_bitonic_desc(float& v, int& i) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
+      const bool lower = (lane & stride) == 0;
+      const bool desc = (lane & size) == 0;   // this segment ends best-first
+      const bool ob = better(ov, oi, v, i);
+      if ((lower == desc) ? ob : !ob) { v = ov; i = oi; }
     }
   }
 }
 
-// One warp per row: chunk maxima and sums, then every chunk's candidates go
-// into per-lane top-k lists (a chunk that overflowed its candidate list is
-// rescanned here, all of it), and a warp merge yields the row's top-k.
 template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(128) vocab_stream_merge_kernel(
+__global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
     const StreamPart* __restrict__ part, int n_chunks, int rows, const T* __restrict__ logits, int V,
     int64_t ld, const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_val, float* __restrict__ row_max,
     float* __restrict__ row_lse) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  __shared__ float s_bv[kMergeWarps][kMergeBuf];
+  __shared__ int s_bi[kMergeWarps][kMergeBuf];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int row = blockIdx.x * kMergeWarps + wl;
   if (row >= rows) return;
   const int src = row_idx ? row_idx[row] : row;
-  const StreamPart* p = part + static_cast<int64_t>(row) * n_chunks;
+  const int dst = src;
+  const StreamPart* gp = part + static_cast<int64_t>(row) * n_chunks;
+  const T* x = logits + static_cast<int64_t>(src) * ld;
+  auto logit = [&](int e) -> float {
+    if constexpr (sizeof(T) == 2) return bf16_at(reinterpret_cast<const uint16_t*>(x) + e);
+    else return reinterpret_cast<const float*>(x)[e];
+  };
+  auto emit_head = [&](int arg, float M, float S) {
+    argmax[dst] = arg;
+    if (row_max) row_max[dst] = M;
+    if (LSE && row_lse) row_lse[dst] = M + logf(S);
+  };
+
+  if (n_chunks <= 32) {
+    float mc = -INFINITY, sc = 0.f;
+    int cc = 0, oc = 0;
+    if (lane < n_chunks) {
+      const uint4 h = *reinterpret_cast<const uint4*>(gp + lane);
+      mc = __uint_as_float(h.x); sc = __uint_as_float(h.y);
+      cc = static_cast<int>(h.z); oc = static_cast<int>(h.w);
+    }
+    const float M = redux_max(mc);
+    float S = 0.f;
+    if (LSE) S = warp_sum(mc != -INFINITY ? sc * ex2((mc - M) * kLog2e) : 0.f);
+    const float tau = KMAX == 1 ? M : (n_chunks >= KMAX ? warp_kth_largest(mc, KMAX) : -INFINITY);
+    const unsigned surv = __ballot_sync(0xffffffffu, lane < n_chunks && mc >= tau);
+    const unsigned ovfm = __ballot_sync(0xffffffffu, oc != 0);
+    int nb = 0;   // buffered candidates, warp-uniform
+    auto append = [&](bool keep, float v, int e) {
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      const int pos = nb + __popc(bal & ((1u << lane) - 1u));
+      if (keep && pos < kMergeBuf) { s_bv[wl][pos] = v; s_bi[wl][pos] = e; }
+      nb += __popc(bal);
+    };
+    // stored candidates of the opened chunks, four chunks' loads in flight
+    unsigned todo = surv & ~ovfm;
+    while (todo) {
+      int cs[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        cs[u] = todo ? __ffs(todo) - 1 : -1;
+        todo &= todo - 1u;
+      }
+      float vv[4];
+      int ii[4];
+      bool kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = __shfl_sync(0xffffffffu, cc, cs[u] & 31);
+        kk[u] = cs[u] >= 0 && lane < n;
+        vv[u] = -INFINITY;
+        ii[u] = INT32_MAX;
+        if (kk[u]) { vv[u] = gp[cs[u]].val[lane]; ii[u] = gp[cs[u]].idx[lane]; }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) append(kk[u] && vv[u] >= tau, vv[u], ii[u]);
+    }
+    // opened chunks whose candidate list overflowed: rescan their logits
+    unsigned rescan = surv & ovfm;
+    while (rescan && nb <= kMergeBuf) {
+      const int c = __ffs(rescan) - 1;
+      rescan &= rescan - 1u;
+      const int e1 = min(V, (c + 1) * kVChunk);
+      for (int e0 = c * kVChunk; e0 < e1 && nb <= kMergeBuf; e0 += 32) {
+        const int e = e0 + lane;
+        const float xv = e < e1 ? logit(e) : -INFINITY;
+        append(e < e1 && xv >= tau, xv, e);
+      }
+    }
+    __syncwarp();
+    if (nb <= 32) {
+      float v = lane < nb ? s_bv[wl][lane] : -INFINITY;
+      int i = lane < nb ? s_bi[wl][lane] : INT32_MAX;
+      warp_bitonic_desc(v, i);
+      const int arg = __shfl_sync(0xffffffffu, i, 0);
+      if (lane == 0) emit_head(arg, M, S);
+      if (k > 0 && lane < k) {
+        if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = i;
+        if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = v;
+      }
+      return;
+    }
+    if (nb <= kMergeBuf) {
+      float lv[KMAX];
+      int li[KMAX];
+#pragma unroll
+      for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
+      for (int t = lane; t < nb; t += 32) list_insert<KMAX>(lv, li, s_bv[wl][t], s_bi[wl][t]);
+      float ov[KMAX];
+      int oi[KMAX];
+      warp_merge_lists<KMAX>(lv, li, ov, oi);
+      if (lane == 0) emit_head(oi[0], M, S);
+      if (k > 0 && lane < k) {
+        float val = ov[0];
+        int idx = oi[0];
+#pragma unroll
+        for (int q = 1; q < KMAX; ++q)
+          if (lane == q) { val = ov[q]; idx = oi[q]; }
+        if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = idx;
+        if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = val;
+      }
+      return;
+    }
+  }
+
+  // plain path: every record, every overflowed chunk rescanned in full
   float M = -INFINITY;
-  for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, p[c].m);
+  for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, gp[c].m);
   M = warp_max(M);
   float S = 0.f;
   if (LSE) {
-    for (int c = lane; c < n_chunks; c += 32) S += p[c].s * ex2((p[c].m - M) * kLog2e);
+    for (int c = lane; c < n_chunks; c += 32)
+      if (gp[c].m != -INFINITY) S += gp[c].s * ex2((gp[c].m - M) * kLog2e);
     S = warp_sum(S);
   }
   float lv[KMAX];
   int li[KMAX];
 #pragma unroll
   for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
-  const T* x = logits + static_cast<int64_t>(src) * ld;
   for (int c = 0; c < n_chunks; ++c) {
-    if (!p[c].ovf) {
-      if (lane < p[c].cnt) list_insert<KMAX>(lv, li, p[c].val[lane], p[c].idx[lane]);
+    if (!gp[c].ovf) {
+      if (lane < gp[c].cnt) list_insert<KMAX>(lv, li, gp[c].val[lane], gp[c].idx[lane]);
     } else {
       const int e1 = min(V, (c + 1) * kVChunk);
-      for (int e = c * kVChunk + lane; e < e1; e += 32) {
-        float xv;
-        if constexpr (sizeof(T) == 2) xv = bf16_at(reinterpret_cast<const uint16_t*>(x) + e);
-        else xv = reinterpret_cast<const float*>(x)[e];
-        list_insert<KMAX>(lv, li, xv, e);
-      }
+      for (int e = c * kVChunk + lane; e < e1; e += 32) list_insert<KMAX>(lv, li, logit(e), e);
     }
   }
   float ov[KMAX];
   int oi[KMAX];
   warp_merge_lists<KMAX>(lv, li, ov, oi);
-  const int dst = src;
-  if (lane == 0) {
-    argmax[dst] = oi[0];
-    if (row_max) row_max[dst] = M;
-    if (LSE && row_lse) row_lse[dst] = M + logf(S);
-  }
+  if (lane == 0) emit_head(oi[0], M, S);
   if (k > 0 && lane < k) {
     float val = ov[0];
     int idx = oi[0];
@@ -592,6 +797,7 @@ __global__ void __launch_bounds__(128) vocab_stream_merge_kernel(
     if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = val;
   }
 }
+
 
 int sm_count_cached() {
   static const int n = [] {
@@ -624,8 +830,7 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
     auto* sp = reinterpret_cast<StreamPart*>(ws);
     vocab_stream_kernel<T, KMAX, LSE><<<grid, kVThreads, smem, st>>>(logits, V, ld, row_idx, rows, n_chunks,
                                                                       sp, nullptr);
-    const int wpb = 4;
-    vocab_stream_merge_kernel<T, KMAX, LSE><<<(rows + wpb - 1) / wpb, 32 * wpb, 0, st>>>(
+    vocab_stream_merge_kernel<T, KMAX, LSE><<<(rows + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
         sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax, topk_idx, topk_val, row_max, row_lse);
     return launch_status();
   }

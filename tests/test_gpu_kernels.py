@@ -317,11 +317,29 @@ def test_retrieve_bad_table_entry_flags_error(tv):
 
 
 # ---------------------------------------------------------------------- D-cut
-@pytest.mark.parametrize("which", ["workload", "ties", "tiny"])
+@pytest.mark.parametrize("which", ["workload", "ties", "tiny", "t1500", "t4000", "t8192", "d0",
+                                   "rho8", "nonmonotone"])
 def test_dcut_select(tv, which):
+    rng = np.random.default_rng(len(which))
+    beta = lambda b, d: rng.beta(4.0, 1.5, (b, d)).astype(np.float32)
+    rhos = list(synth.DCUT_RHOS)
     if which == "workload":
         conf = synth.dcut_batch(with_attention=False, with_logits=False)["conf"]
-        rhos = list(synth.DCUT_RHOS)
+    elif which == "t1500":     # two keys per thread in the sorting network
+        conf = beta(100, 14)
+    elif which == "t4000":     # four keys per thread
+        conf = beta(200, 19)
+    elif which == "t8192":     # the largest batch the kernel takes
+        conf = beta(512, 15)
+    elif which == "d0":        # root-only requests: every score is 1, order = position
+        conf = np.zeros((5000, 0), np.float32)
+        rhos = [0.0, 0.3, 0.5001, 1.0]
+    elif which == "rho8":      # the most budgets one call takes
+        conf = beta(37, 20)
+        rhos = [0.0, 0.01, 0.1, 0.25, 0.5, 0.75, 0.99, 1.0]
+    elif which == "nonmonotone":   # confidences above 1: kept sets are not prefixes
+        conf = rng.uniform(0.0, 2.0, (125, 15)).astype(np.float32)
+        rhos = [0.2, 0.5, 0.8]
     elif which == "ties":
         rng = np.random.default_rng(5)
         conf = rng.choice(np.array([1.0, 0.5, 0.25, 0.75], np.float32), (40, 9))
