@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(128) vocab_merge_kernel(
 // record.  Nothing is ranked per chunk: the per-row merge ranks all
 // candidates, so a chunk costs one block barrier and no serial section.
 // ---------------------------------------------------------------------------
-// ring of 8192-element chunks: 4 x 16 KB for bf16, 3 x 32 KB for fp32
+// ring of 8192-element chunks: 4 x 16 KB for bf16 (three CTAs per SM), 3 x 32 KB for fp32
 template <typename T> constexpr int stream_stages() { return sizeof(T) == 2 ? 4 : 3; }
 template <typename T> constexpr int stream_chunk_bytes() { return kVChunk * static_cast<int>(sizeof(T)); }
 
@@ -443,94 +443,165 @@ __device__ __forceinline__ float warp_kth_largest(float v, int k) {
 // near k (about 9 for k = 8 on Gaussian logits) and far below kSCand.
 template <int KMAX> constexpr int tau_per_warp() { return KMAX == 1 ? 1 : (KMAX <= 8 ? 2 : 4); }
 
+// Chunk max and top-k threshold from the NV = NW * P collected thread maxima
+// (s_top, 16-byte aligned): every lane reads them all with broadcast loads,
+// lane l < NV ranks value l by (value desc, slot asc), and tau is the value of
+// rank KMAX - 1.  Independent compares instead of a chain of warp reductions.
+template <int NV, int KMAX>
+__device__ __forceinline__ void chunk_max_tau(const float* s_top, float& M, float& tau) {
+  static_assert(NV % 4 == 0 && NV <= 32, "threshold values: a multiple of 4, one warp");
+  const int lane = threadIdx.x & 31;
+  float t[NV];
+#pragma unroll
+  for (int q = 0; q < NV / 4; ++q) {
+    const float4 w = reinterpret_cast<const float4*>(s_top)[q];
+    t[4 * q] = w.x; t[4 * q + 1] = w.y; t[4 * q + 2] = w.z; t[4 * q + 3] = w.w;
+  }
+  float m = t[0];
+#pragma unroll
+  for (int q = 1; q < NV; ++q) m = fmaxf(m, t[q]);
+  M = m;
+  if (KMAX == 1) {
+    tau = m;
+    return;
+  }
+  const int l = lane < NV ? lane : 0;
+  const float mine = s_top[l];
+  int rank = 0;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) rank += (t[q] > mine) | ((t[q] == mine) & (q < l));
+  const unsigned sel = __ballot_sync(0xffffffffu, lane < NV && rank == KMAX - 1);
+  tau = __shfl_sync(0xffffffffu, mine, __ffs(sel) - 1);
+}
+
+__device__ __forceinline__ void bar_named(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool bar_named_and(int id, int n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\tbar.red.and.pred b, %2, %3, a;\n\tselp.u32 %0, 1, 0, b;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_arrive_plain(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Workspace header of the streaming path (zeroed before every launch).
+struct StreamHdr {
+  int status;   // nonzero: a wait ran out
+  int claim;    // next unclaimed (row, chunk) item
+};
+constexpr size_t kStreamHdrBytes = 256;
+
+// CTA = 8 compute warps + 1 producer warp.  The producer's lane 0 claims
+// (row, chunk) items from a global counter, so SMs that run slower simply
+// take fewer items, and copies each into the next free ring slot; compute
+// warps never wait on its memory round trips.  Per item the compute warps
+// take thread maxima (bf16 pairs at a time), each warp's top P thread
+// maxima, one named barrier, then the chunk max and threshold tau (k-th
+// largest of the 8 P values: at least k distinct elements are >= tau) and
+// the candidates >= tau, reread from the slot.  After the barrier of item i
+// thread 0 frees the slot of item i - 1 and closes that item's record (its
+// candidates are final there).
+constexpr int kStreamThreads = kVThreads + 32;
+
 template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
+__global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
     const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows,
-    int n_chunks, StreamPart* __restrict__ part, int* __restrict__ err) {
+    int n_chunks, StreamPart* __restrict__ part, StreamHdr* __restrict__ hdr) {
   constexpr int EPT = kVPerThread;                        // 32 values per thread
   constexpr int VEC = 16 / static_cast<int>(sizeof(T));   // elements per 16 B
   constexpr int CH = kVChunk;                             // 8192 elements per chunk
   constexpr int NW = kVThreads / 32;
   constexpr int P = tau_per_warp<KMAX>();
-  static_assert(NW * P <= 32, "threshold values must fit one warp");
-  constexpr int kSStages = stream_stages<T>();
+  constexpr int NV = NW * P;
+  constexpr int S = stream_stages<T>();
   constexpr int kSChunkBytes = stream_chunk_bytes<T>();
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[4];
-  // double-buffered by item parity: item i writes buffer i & 1 before the
-  // block barrier of item i and it is read after it, so one barrier per item
-  // suffices
-  __shared__ float s_top[2][NW * P];
+  __shared__ __align__(8) uint64_t full[S], empty[S];
+  __shared__ int s_item[S], s_chunk[S];
+  __shared__ __align__(16) float s_top[2][NV];
   __shared__ float s_wsum[2][NW];
   __shared__ int s_cnt[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
-  const int G = gridDim.x;
   if (tid == 0) {
-    for (int s = 0; s < kSStages; ++s)
+    for (int s = 0; s < S; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&empty[s])) : "memory");
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_cnt[0] = s_cnt[1] = 0;
   }
   __syncthreads();
-  auto issue = [&](int item, int s) {
-    const int row = item / n_chunks, c = item - row * n_chunks;
-    const int src = row_idx ? row_idx[row] : row;
-    const int n = min(CH, V - c * CH);
-    bulk_g2s(sm_u32(ring + s * kSChunkBytes), logits + static_cast<int64_t>(src) * ld + static_cast<int64_t>(c) * CH,
-             static_cast<uint32_t>(n * sizeof(T)), sm_u32(&full[s]));
-  };
-  if (tid == 0)
-    for (int s = 0; s < kSStages; ++s)
-      if (static_cast<int>(blockIdx.x) + s * G < items) issue(blockIdx.x + s * G, s);
 
-  // thread 0 closes an item's record one item later, once all its candidates are in
-  float rec_m = 0.f, rec_s = 0.f;
-  auto close_record = [&](int item, int buf) {
-    StreamPart* o = part + item;
-    const int cnt = s_cnt[buf];
-    s_cnt[buf] = 0;
-    o->m = rec_m;
-    o->s = rec_s;
-    o->cnt = min(cnt, kSCand);
-    o->ovf = cnt > kSCand;
-  };
+  if (warp == NW) {   // ------------------------------------------------ producer
+    if (lane != 0) return;
+    // two claims in flight: the item for this slot and the next one
+    int a0 = atomicAdd(&hdr->claim, 1);
+    int a1 = a0 < items ? atomicAdd(&hdr->claim, 1) : items;
+    for (int q = 0;; ++q) {
+      const int s = q % S;
+      const int item = a0;
+      a0 = a1;
+      if (a1 < items) a1 = atomicAdd(&hdr->claim, 1);
+      if (q >= S && !bar_wait_fast(sm_u32(&empty[s]), ((q / S) - 1) & 1)) {
+        atomicExch(&hdr->status, 1);
+        return;
+      }
+      if (item >= items) {   // no more work: an empty slot tells the compute warps
+        s_item[s] = -1;
+        bar_arrive_plain(sm_u32(&full[s]));
+        return;
+      }
+      const int row = item / n_chunks, c = item - row * n_chunks;
+      const int src = row_idx ? row_idx[row] : row;
+      s_item[s] = item;
+      s_chunk[s] = c;
+      const int n = min(CH, V - c * CH);
+      bulk_g2s(sm_u32(ring + s * kSChunkBytes), logits + static_cast<int64_t>(src) * ld + static_cast<int64_t>(c) * CH,
+               static_cast<uint32_t>(n * sizeof(T)), sm_u32(&full[s]));
+    }
+  }
 
-  const int dc = G % n_chunks;                // chunk index advances by G mod n_chunks
-  int c = blockIdx.x % n_chunks;
-  int it = 0;
-  bool all_ok = true;
-  for (int item = blockIdx.x; item < items; item += G, ++it) {
-    const int s = it % kSStages, b = it & 1;
+  // ------------------------------------------------------------- compute warps
+  float rec_m = 0.f, rec_s = 0.f;   // thread 0: max and sum of the previous item
+  int prev = -1;
+  for (int it = 0;; ++it) {
+    const int s = it % S, b = it & 1;
+    const bool ok = bar_wait_fast(sm_u32(&full[s]), (it / S) & 1);
+    const int item = ok ? s_item[s] : -1;
+    const int c = ok ? s_chunk[s] : 0;
     const int base = c * CH;
-    const int n_valid = min(CH, V - base);
-    const bool ok = bar_wait_fast(sm_u32(&full[s]), (it / kSStages) & 1);
+    const int n_valid = item >= 0 ? min(CH, V - base) : 0;
     const uint8_t* st = ring + s * kSChunkBytes;
-    // bf16 without exponentials on a full chunk: keep the packed pairs and
-    // take the maximum two at a time; otherwise unpack to fp32
-    const bool packed = sizeof(T) == 2 && !LSE && ok && n_valid == CH;
-    float v[EPT];
-    uint32_t raw[EPT / 2];
     float my_max;
-    if (packed) {
-      __nv_bfloat162 pm = __float2bfloat162_rn(-INFINITY);
+    float v[EPT];
+    if (sizeof(T) == 2 && !LSE && n_valid == CH) {
+      __nv_bfloat162 pm[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
-        raw[4 * j] = w.x; raw[4 * j + 1] = w.y; raw[4 * j + 2] = w.z; raw[4 * j + 3] = w.w;
+        pm[j] = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x),
+                                *reinterpret_cast<const __nv_bfloat162*>(&w.y)),
+                        __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z),
+                                *reinterpret_cast<const __nv_bfloat162*>(&w.w)));
       }
-#pragma unroll
-      for (int q = 0; q < EPT / 2; ++q) pm = __hmax2(pm, *reinterpret_cast<const __nv_bfloat162*>(&raw[q]));
-      my_max = fmaxf(__low2float(pm), __high2float(pm));
+      const __nv_bfloat162 m2 = __hmax2(__hmax2(pm[0], pm[1]), __hmax2(pm[2], pm[3]));
+      my_max = fmaxf(__low2float(m2), __high2float(m2));
     } else {
-      if (ok && n_valid == CH) stage_values<T, false>(st, CH, v);
-      else stage_values<T, true>(st, ok ? n_valid : 0, v);
-      my_max = v[0];
+      if (n_valid == CH) stage_values<T, false>(st, CH, v);
+      else stage_values<T, true>(st, n_valid, v);
+      float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int t = 1; t < EPT; ++t) my_max = fmaxf(my_max, v[t]);
+      for (int t = 4; t < EPT; ++t) m4[t & 3] = fmaxf(m4[t & 3], v[t]);
+      my_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
     }
-    // per-warp top-P thread maxima
     const float wmax = redux_max(my_max);
     if (lane == 0) s_top[b][warp * P] = wmax;
     if constexpr (P > 1) {
@@ -553,16 +624,27 @@ __global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
       sum = warp_sum(sum);
       if (lane == 0) s_wsum[b][warp] = sum;
     }
-    all_ok = __syncthreads_and(ok) != 0;   // block-uniform outcome of the wait
-    // every read of ring slot s happened before the barrier: refill it now
-    if (tid == 0) {
-      if (it > 0) close_record(item - G, b ^ 1);
-      if (all_ok && item + kSStages * G < items) issue(item + kSStages * G, s);
+    const bool all_ok = bar_named_and(1, kVThreads, ok);   // block-uniform
+    if (!all_ok) {
+      if (tid == 0) atomicExch(&hdr->status, 1);
+      return;
     }
-    if (!all_ok) break;
-    const float tv = lane < NW * P ? s_top[b][lane] : -INFINITY;
-    const float M = redux_max(tv);
-    const float tau = KMAX == 1 ? M : warp_kth_largest(tv, KMAX);
+    if (tid == 0) {
+      // the previous item's slot was last read (candidate pass) before this barrier
+      if (it > 0) bar_arrive_plain(sm_u32(&empty[(it - 1) % S]));
+      if (prev >= 0) {                        // candidates of the previous item are final
+        StreamPart* o = part + prev;
+        const int cnt = s_cnt[b ^ 1];
+        s_cnt[b ^ 1] = 0;
+        o->m = rec_m;
+        o->s = rec_s;
+        o->cnt = min(cnt, kSCand);
+        o->ovf = cnt > kSCand;
+      }
+    }
+    if (item < 0) return;
+    float M, tau;
+    chunk_max_tau<NV, KMAX>(s_top[b], M, tau);
     if (tid == 0) {
       float ssum = 0.f;
       if constexpr (LSE) {
@@ -575,6 +657,7 @@ __global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
       rec_m = M;
       rec_s = ssum;
     }
+    prev = item;
     if (my_max >= tau) {
       StreamPart* out = part + item;
       auto put = [&](float val, int e) {
@@ -584,16 +667,22 @@ __global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
           out->idx[pos] = base + e;
         }
       };
-      if (packed) {
+      if (sizeof(T) == 2 && !LSE && n_valid == CH) {
+        // reread this thread's values (the slot is freed at the next barrier);
         // tau is one of the chunk's elements, so exact in bf16
         const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
 #pragma unroll
-        for (int q = 0; q < EPT / 2; ++q) {
-          const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&raw[q]), t2);
-          if (msk) {
-            const int e = ((q / 4) * kVThreads + tid) * VEC + 2 * (q % 4);
-            if (msk & 0xffffu) put(bf16_lo(raw[q]), e);
-            if (msk >> 16) put(bf16_hi(raw[q]), e + 1);
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q]), t2);
+            if (msk) {
+              const int e = (j * kVThreads + tid) * VEC + 2 * q;
+              if (msk & 0xffffu) put(bf16_lo(ws[q]), e);
+              if (msk >> 16) put(bf16_hi(ws[q]), e + 1);
+            }
           }
         }
       } else {
@@ -602,15 +691,7 @@ __global__ void __launch_bounds__(kVThreads, 3) vocab_stream_kernel(
           if (v[t] >= tau) put(v[t], ((t / VEC) * kVThreads + tid) * VEC + (t % VEC));
       }
     }
-    c += dc;
-    if (c >= n_chunks) c -= n_chunks;
   }
-  if (!all_ok) {
-    if (tid == 0 && err) *err = 1;
-    return;
-  }
-  __syncthreads();
-  if (tid == 0 && it > 0) close_record(blockIdx.x + (it - 1) * G, (it - 1) & 1);
 }
 
 // One warp per row.  The warp reads the row's chunk headers (max, sum,
@@ -825,11 +906,12 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
                                                   smem) == cudaSuccess;
     if (!attr) return TV_ECUDA;
     const int items = rows * n_chunks;
-    const int per_sm = sizeof(T) == 2 ? 3 : 2;
-    const int grid = std::min(items, per_sm * sm_count_cached());
-    auto* sp = reinterpret_cast<StreamPart*>(ws);
-    vocab_stream_kernel<T, KMAX, LSE><<<grid, kVThreads, smem, st>>>(logits, V, ld, row_idx, rows, n_chunks,
-                                                                      sp, nullptr);
+    const int grid = std::min(items, 3 * sm_count_cached());
+    auto* hdr = reinterpret_cast<StreamHdr*>(ws);
+    auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
+    if (cudaMemsetAsync(hdr, 0, sizeof(StreamHdr), st) != cudaSuccess) return TV_ECUDA;
+    vocab_stream_kernel<T, KMAX, LSE><<<grid, kStreamThreads, smem, st>>>(logits, V, ld, row_idx, rows, n_chunks,
+                                                                           sp, hdr);
     vocab_stream_merge_kernel<T, KMAX, LSE><<<(rows + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
         sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax, topk_idx, topk_val, row_max, row_lse);
     return launch_status();
@@ -865,7 +947,7 @@ TV_API size_t vocab_argmax_topk_workspace_size(int rows, int V, int k) {
   const size_t n_chunks = (static_cast<size_t>(V) + tv::kVChunk - 1) / tv::kVChunk;
   const size_t kmax = k <= 1 ? 1 : (k <= 8 ? 8 : 16);
   const size_t part = std::max(2 * sizeof(float) + kmax * (sizeof(float) + sizeof(int)), sizeof(tv::StreamPart));
-  return static_cast<size_t>(rows) * n_chunks * part;
+  return tv::kStreamHdrBytes + static_cast<size_t>(rows) * n_chunks * part;
 }
 
 TV_API int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld,
