@@ -169,21 +169,22 @@ int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld
  * serving hot path (cudaMalloc can synchronise the device and can fail under
  * memory pressure), and code that must not change allocator state.  This
  * entry point needs no workspace: its scratch is a file-scope device array of
- * TV_NOALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads the library
+ * TV_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
  * holds until the process exits.  Arguments and outputs are those of
  * vocab_argmax_topk; the caller still provides the inputs and outputs.
  *   - Sizes whose scratch need (vocab_argmax_topk_workspace_size) exceeds
  *     TV_NOALLOC_SCRATCH_BYTES are rejected with TV_EWORKSPACE (for V = 151936:
- *     up to 1623 rows).
+ *     up to 1698 rows).
  *   - The first call on a device looks up the array's device address (one
  *     runtime query, no allocation); make that first call before any stream
  *     capture on that device.
  *   - All calls share the one array and it keeps the last call's contents
- *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     (nothing in it needs to start at zero: each call clears the small
+ *     header it uses with an asynchronous memset on the given stream).  Calls that overlap on the GPU
  *     (different streams without ordering) race on it: order them.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * -------------------------------------------------------------------------- */
-#define TV_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define TV_NOALLOC_SCRATCH_BYTES (32u << 20)
 int vocab_argmax_topk_noalloc(const void* logits, int dtype, int rows, int V, int64_t ld,
                               const int32_t* row_idx, int k, int32_t* argmax, int32_t* topk_idx,
                               float* topk_val, float* row_max, float* row_lse, tv_stream_t stream);

@@ -26,6 +26,14 @@ struct AttnParams {
   int B, max_nodes, max_prefix, Hq, Hkv, d, dtype;
   float scale;
   int n_split;
+  // Tensor-core work plan: unit z of the grid covers keys [piece * piece_len,
+  // (piece + 1) * piece_len) of request r, the last piece also the tree
+  // block; the pieces of one (request, KV head, tile) are merged by the last
+  // of them to finish.  Units are ordered longest first.
+  const int4* plan;    // [n_units] (r, piece, n_pieces, 0); r < 0: no work
+  int* piece_cnt;      // [B * Hkv * tiles] finished pieces, zeroed by the planner
+  int piece_len;       // keys per piece, a multiple of 64
+  int n_units;
 };
 
 int attn_simt(const AttnParams& p, cudaStream_t st);
@@ -35,7 +43,11 @@ int attn_combine(const AttnParams& p, cudaStream_t st);
 
 // Tensor-core path: bf16, head_dim 128, Hq/Hkv dividing 128.
 bool attn_tc_supported(int dtype, int d, int Hq, int Hkv);
-int attn_tc_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm);
+// Piece length and the most pieces per request for a call's sizes (also
+// sizes the workspace): requests are split into pieces only when whole
+// requests are too few to fill the resident CTAs.
+void attn_tc_shape(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm, int* piece_len,
+                   int* max_pieces, int* tiles);
 int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st);
 
 }  // namespace tv

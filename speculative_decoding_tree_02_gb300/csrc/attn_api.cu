@@ -30,23 +30,33 @@ bool use_tc(int dtype, int d, int Hq, int Hkv) {
 
 struct WsLayout {
   bool tc;
-  int n_split;
-  size_t status, o_bytes, ml_bytes, total;
+  int n_split;                               // SIMT path
+  int piece_len, max_pieces, tiles, n_units;  // tensor-core path
+  size_t status, plan, cnt, o_bytes, ml_bytes, total;
 };
 
-// [status word (256 B)] [split partials o] [split partials (m, l)]
+// SIMT:        [status word (256 B)] [split partials o] [split partials (m, l)]
+// tensor core: [status word (256 B)] [work plan] [piece counters]
+//              [piece partials o] [piece partials (m, l)]
 WsLayout ws_layout(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int d, int dtype) {
   WsLayout w{};
   w.tc = use_tc(dtype, d, Hq, Hkv);
-  w.n_split = w.tc ? tv::attn_tc_splits(B, max_nodes, max_prefix, Hq, Hkv, sm_count())
-                   : tv::attn_simt_splits(B, max_nodes, max_prefix, Hq, Hkv, sm_count());
   w.status = 256;
-  if (w.n_split > 1) {
-    const size_t rows = static_cast<size_t>(w.n_split) * B * max_nodes * Hq;
-    w.o_bytes = align256(rows * d * sizeof(float));
-    w.ml_bytes = align256(rows * sizeof(float2));
+  size_t parts = 0;   // partial rows
+  if (w.tc) {
+    tv::attn_tc_shape(B, max_nodes, max_prefix, Hq, Hkv, sm_count(), &w.piece_len, &w.max_pieces, &w.tiles);
+    w.n_split = 1;
+    w.n_units = B * w.max_pieces;
+    w.plan = align256(static_cast<size_t>(w.n_units) * sizeof(int4));
+    w.cnt = align256(static_cast<size_t>(B) * Hkv * w.tiles * sizeof(int));
+    if (w.max_pieces > 1) parts = static_cast<size_t>(w.max_pieces) * B * max_nodes * Hq;
+  } else {
+    w.n_split = tv::attn_simt_splits(B, max_nodes, max_prefix, Hq, Hkv, sm_count());
+    if (w.n_split > 1) parts = static_cast<size_t>(w.n_split) * B * max_nodes * Hq;
   }
-  w.total = w.status + w.o_bytes + w.ml_bytes;
+  w.o_bytes = align256(parts * d * sizeof(float));
+  w.ml_bytes = align256(parts * sizeof(float2));
+  w.total = w.status + w.plan + w.cnt + w.o_bytes + w.ml_bytes;
   return w;
 }
 
@@ -98,13 +108,20 @@ TV_API int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre,
   p.anc_words = anc_words; p.B = B; p.max_nodes = max_nodes; p.max_prefix = max_prefix;
   p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.dtype = dtype; p.scale = scale; p.n_split = w.n_split;
   char* base = static_cast<char*>(ws);
-  if (w.n_split > 1) {
-    p.ws_o = reinterpret_cast<float*>(base + w.status);
-    p.ws_ml = reinterpret_cast<float2*>(base + w.status + w.o_bytes);
+  char* parts = base + w.status + w.plan + w.cnt;
+  if (w.o_bytes) {
+    p.ws_o = reinterpret_cast<float*>(parts);
+    p.ws_ml = reinterpret_cast<float2*>(parts + w.o_bytes);
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* status = reinterpret_cast<int*>(base);
+  if (w.tc) {   // the planner kernel clears the status word and the counters
+    p.plan = reinterpret_cast<const int4*>(base + w.status);
+    p.piece_cnt = reinterpret_cast<int*>(base + w.status + w.plan);
+    p.piece_len = w.piece_len;
+    p.n_units = w.n_units;
+    return tv::attn_tc(p, total_nodes, total_prefix, status, st);
+  }
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return TV_ECUDA;
-  if (w.tc) return tv::attn_tc(p, total_nodes, total_prefix, status, st);
   return tv::attn_simt(p, st);
 }

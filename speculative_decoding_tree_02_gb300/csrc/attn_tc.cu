@@ -243,8 +243,11 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
   const uint32_t sb = smem_u32(sm);
   const AttnParams& p = P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, tile = blockIdx.y;
-  const int r = blockIdx.z / p.Hkv, kvh = blockIdx.z % p.Hkv;
+  const int kvh = blockIdx.x, tile = blockIdx.y;
+  const int4 unit = p.plan[blockIdx.z];
+  const int r = unit.x;
+  if (r < 0) return;                                   // uniform: a unit without work
+  const int piece = unit.y, n_pieces = unit.z;
   const int g = p.Hq / p.Hkv;
   const int nq = LIVE / g;
   const int n0 = p.node_off[r];
@@ -309,11 +312,14 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
   }
 
   // ---- key blocks of this CTA
-  const int chunk = (p.max_prefix + p.n_split - 1) / p.n_split;
-  const int kb = split * chunk;
-  const int ke = min(kb + chunk, vmax);
+  const int kb = piece * p.piece_len;
+  const int ke = min(kb + p.piece_len, vmax);
   const int n_pre = ke > kb ? (ke - kb + kBlk - 1) / kBlk : 0;
-  const bool do_tree = (split == p.n_split - 1) && thi >= 0 && tlo <= thi;
+  const bool do_tree = (piece == n_pieces - 1) && thi >= 0 && tlo <= thi;
+  // partial-output slot of (piece, row)
+  auto pslot = [&](int pc) {
+    return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
+  };
   const int tb = do_tree ? (tlo & ~63) : 0;   // one 64-bit ancestor word per 64-key block
   const int n_tree = do_tree ? (thi + 1 - tb + kBlk - 1) / kBlk : 0;
   const int nblk = n_pre + n_tree;
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
 #pragma unroll
           for (int c = 0; c < 32; ++c) pin(o[c]);
           if (write) {
-            if (p.n_split == 1) {
+            if (n_pieces == 1) {
               uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(gn) * p.Hq + head) * kD + 32 * q;
 #pragma unroll
               for (int c = 0; c < 32; c += 8) {
@@ -579,9 +585,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
                 *reinterpret_cast<uint4*>(op + c) = v4;
               }
             } else {
-              const int64_t slot = (static_cast<int64_t>(split) * p.B * p.max_nodes +
-                                    static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
-              float* po = p.ws_o + slot * kD + 32 * q;
+              float* po = p.ws_o + pslot(piece) * kD + 32 * q;
 #pragma unroll
               for (int c = 0; c < 32; c += 4)
                 *reinterpret_cast<float4*>(po + c) =
@@ -592,28 +596,178 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
         }
       }
       if (write) {
-        if (p.n_split == 1) {
+        if (n_pieces == 1) {
           if (p.lse) p.lse[static_cast<int64_t>(gn) * p.Hq + head] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         } else {
-          const int64_t slot = (static_cast<int64_t>(split) * p.B * p.max_nodes +
-                                static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
-          p.ws_ml[slot] = make_float2(m, l);
+          p.ws_ml[pslot(piece)] = make_float2(m, l);
         }
       }
     }
-  } else if (is_soft && active && p.n_split > 1) {
-    // no keys in this split: an empty partial
-    const int64_t slot = (static_cast<int64_t>(split) * p.B * p.max_nodes +
-                          static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
-    p.ws_ml[slot] = make_float2(-INFINITY, 0.f);
+  } else if (is_soft && active && n_pieces > 1) {
+    // no keys in this piece: an empty partial
+    p.ws_ml[pslot(piece)] = make_float2(-INFINITY, 0.f);
   }
+  if (n_pieces > 1) __threadfence();   // this thread's partial, before the count below
   tc_fence_before();
   __syncthreads();
+  // ---- pieces: the last of a (request, KV head, tile) to finish merges them
+  int* last_flag = red;   // the reduction scratch is free again
+  if (n_pieces > 1 && threadIdx.x == 0) {
+    const int old = atomicAdd(&p.piece_cnt[(static_cast<int64_t>(r) * p.Hkv + kvh) * gridDim.y + tile], 1);
+    *last_flag = old == n_pieces - 1;
+  }
+  if (n_pieces > 1) __syncthreads();
   if (warp == L::kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+  if (n_pieces > 1 && *last_flag) {
+    // merge in piece order: all threads, two per query row (64 columns each)
+    constexpr int kMaxP = 8;   // weights held in registers; more pieces recompute them
+    __threadfence();
+    for (int rr = threadIdx.x >> 1; rr < LIVE; rr += kThreads / 2) {
+      const int mln = node_first + rr / g;
+      if (mln >= cnt) continue;
+      const int mhead = kvh * g + rr % g;
+      const int half = threadIdx.x & 1;
+      auto mslot = [&](int pc) {
+        return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + mln) * p.Hq +
+               mhead;
+      };
+      float2 ml[kMaxP];
+#pragma unroll
+      for (int i = 0; i < kMaxP; ++i) ml[i] = i < n_pieces ? __ldcg(&p.ws_ml[mslot(i)]) : make_float2(-INFINITY, 0.f);
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kMaxP; ++i) M = fmaxf(M, ml[i].x);
+      for (int i = kMaxP; i < n_pieces; ++i) M = fmaxf(M, __ldcg(&p.ws_ml[mslot(i)].x));
+      float W = 0.f;
+      float acc[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+      auto add_piece = [&](float2 mi, int i) {
+        const float w = mi.y > 0.f ? ex2(mi.x - M) * mi.y : 0.f;   // empty piece: weight 0
+        W += w;
+        const float4* po = reinterpret_cast<const float4*>(p.ws_o + mslot(i) * kD + 64 * half);
+        float4 o4[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o4[c] = __ldcg(po + c);
+        if (w == 0.f) return;   // (an empty piece's o was never written)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          acc[4 * c] = fmaf(w, o4[c].x, acc[4 * c]);
+          acc[4 * c + 1] = fmaf(w, o4[c].y, acc[4 * c + 1]);
+          acc[4 * c + 2] = fmaf(w, o4[c].z, acc[4 * c + 2]);
+          acc[4 * c + 3] = fmaf(w, o4[c].w, acc[4 * c + 3]);
+        }
+      };
+#pragma unroll
+      for (int i = 0; i < kMaxP; ++i)
+        if (i < n_pieces) add_piece(ml[i], i);
+      for (int i = kMaxP; i < n_pieces; ++i) add_piece(__ldcg(&p.ws_ml[mslot(i)]), i);
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(n0 + mln) * p.Hq + mhead) * kD + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 64; c += 8) {
+        const uint4 v4 = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv), pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
+                                    pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
+        *reinterpret_cast<uint4*>(op + c) = v4;
+      }
+      if (half == 0 && p.lse)
+        p.lse[static_cast<int64_t>(n0 + mln) * p.Hq + mhead] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+// Work plan (one CTA): request r gets n_r = max(1, ceil(P_r / piece_len))
+// pieces.  Units [0, F) are the full pieces (length piece_len) of every
+// request in (r, piece) order, F = sum (n_r - 1); units [F, F + B) are the
+// last pieces by decreasing length (64-key buckets; order within a bucket is
+// free: the merge runs in piece order whatever the schedule); the rest have
+// no work.  Also zeroes the status word and the piece counters.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 1024;
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* __restrict__ pre_off, int B,
+                                                                 int piece_len, int max_pieces, int n_units,
+                                                                 int4* __restrict__ plan,
+                                                                 int* __restrict__ piece_cnt, int n_cnt,
+                                                                 int* __restrict__ status) {
+  __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets], s_w[33];
+  __shared__ int s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) { *status = 0; s_base = 0; }
+  for (int i = tid; i < n_cnt; i += kPlanThreads) piece_cnt[i] = 0;
+  for (int i = tid; i < kPlanBuckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
+  __syncthreads();
+  auto shape = [&](int r, int& n, int& bucket) {
+    const int Pr = pre_off[r + 1] - pre_off[r];
+    n = Pr > 0 ? min((Pr + piece_len - 1) / piece_len, max_pieces) : 1;   // keys past max_prefix: none
+    const int last = Pr - (n - 1) * piece_len;
+    bucket = min(kPlanBuckets - 1, (last + 63) / 64);
+  };
+  for (int r = tid; r < B; r += kPlanThreads) {
+    int n, bk;
+    shape(r, n, bk);
+    atomicAdd(&s_hist[bk], 1);
+  }
+  __syncthreads();
+  // bucket starts in decreasing-length order (one warp, suffix sums)
+  if (warp == 0) {
+    int carry = 0;
+    for (int b0 = kPlanBuckets - 32; b0 >= 0; b0 -= 32) {
+      const int b = b0 + 31 - lane;          // lane 0 takes the longest bucket of the group
+      int v = s_hist[b], x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_fill[b] = carry + x - v;             // units of longer buckets before this one
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  __syncthreads();
+  // full pieces: exclusive scan of (n_r - 1) over requests, in chunks of the block
+  for (int r0 = 0; r0 < B; r0 += kPlanThreads) {
+    const int r = r0 + tid;
+    int n = 1, bk = 0;
+    if (r < B) shape(r, n, bk);
+    const int full = n - 1;
+    int x = full;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = s_w[lane];
+      int iw = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, iw, o);
+        if (lane >= o) iw += y;
+      }
+      s_w[lane] = iw - w;
+      if (lane == 31) s_w[32] = iw;
+    }
+    __syncthreads();
+    const int start = s_base + s_w[warp] + x - full;
+    for (int pc = 0; pc < full; ++pc) plan[start + pc] = make_int4(r, pc, n, 0);
+    __syncthreads();
+    if (tid == 0) s_base += s_w[32];
+    __syncthreads();
+  }
+  const int F = s_base;
+  for (int r = tid; r < B; r += kPlanThreads) {
+    int n, bk;
+    shape(r, n, bk);
+    const int pos = F + s_fill[bk] + atomicAdd(&s_hist[bk], -1) - 1;   // any slot of the bucket
+    plan[pos] = make_int4(r, n - 1, n, 0);
+  }
+  for (int u = F + B + tid; u < n_units; u += kPlanThreads) plan[u] = make_int4(-1, 0, 0, 0);
 }
 
 // ------------------------------------------------------------------ host side
@@ -655,17 +809,30 @@ bool attn_tc_supported(int dtype, int d, int Hq, int Hkv) {
 // 64 live rows when a whole request fits in one 64-row tile, else 128
 static int tc_live(int max_nodes, int g) { return static_cast<long long>(max_nodes) * g <= 64 ? 64 : 128; }
 
-int attn_tc_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm) {
+void attn_tc_shape(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_sm, int* piece_len,
+                   int* max_pieces, int* tiles) {
   const int g = Hq / Hkv;
   const int live = tc_live(max_nodes, g);
   const int nq = live / g;
-  const long long tiles = (max_nodes + nq - 1) / nq;
-  const long long base = static_cast<long long>(B) * Hkv * tiles;
+  *tiles = (max_nodes + nq - 1) / nq;
   const long long slots = static_cast<long long>(n_sm) * (live == 64 ? 2 : 1);   // resident CTAs
-  long long s = (2LL * slots + base - 1) / base;
-  if (base >= slots) s = 1;
-  s = std::min<long long>(s, std::max(1, (max_prefix + 511) / 512));
-  return static_cast<int>(std::max(1LL, std::min(s, 64LL)));
+  // Enough (request, KV head, tile) units to fill the resident slots: whole
+  // requests, longest first (a piece split costs a partial round trip and a
+  // merge, more than the tail it removes).  Fewer: pieces sized so that the
+  // units about fill the slots.
+  const long long units = static_cast<long long>(B) * Hkv * *tiles;
+  long long L = std::max(64, (max_prefix + 63) / 64 * 64);
+  if (units < slots && max_prefix > 512) {
+    const long long keys = units * max_prefix;
+    L = std::max<long long>(512, ((keys + slots - 1) / slots + 63) / 64 * 64);
+  }
+  long long mp = max_prefix > 0 ? (max_prefix + L - 1) / L : 1;
+  while (static_cast<long long>(B) * mp > 65535) {   // grid z limit
+    L *= 2;
+    mp = (max_prefix + L - 1) / L;
+  }
+  *piece_len = static_cast<int>(std::min<long long>(L, 1LL << 30));
+  *max_pieces = static_cast<int>(std::max(1LL, mp));
 }
 
 template <int LIVE>
@@ -693,9 +860,10 @@ static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long 
   }
   if (!ok) return TV_ECUDA;
   const int tiles = (p.max_nodes + nq - 1) / nq;
-  dim3 grid(p.n_split, tiles, p.B * p.Hkv);
+  tc::attn_plan_kernel<<<1, tc::kPlanThreads, 0, st>>>(p.pre_off, p.B, p.piece_len, p.n_units / p.B, p.n_units,
+                                                       const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles, err);
+  dim3 grid(p.Hkv, tiles, p.n_units);
   tc::attn_tc_kernel<LIVE><<<grid, L::kThreads, L::kSmemBytes, st>>>(P);
-  if (p.n_split > 1) return attn_combine(p, st);
   return launch_status();
 }
 

@@ -406,7 +406,10 @@ __device__ __forceinline__ void stage_values(const uint8_t* st, int n_valid, flo
 
 // Partial of one streamed chunk: max, sum of exp(x - max), and every element
 // >= the chunk threshold (up to kSCand of them; ovf = 1 when there were more).
-constexpr int kSCand = 32;
+// The threshold below leaves about 22 candidates per chunk on Gaussian
+// logits for k <= 8; more than 128 occurred in none of 2 * 10^5 simulated
+// chunks (more than 96: 3 * 10^-5 of them).
+constexpr int kSCand = 128;
 struct StreamPart {
   float m, s;
   int cnt, ovf;
@@ -418,10 +421,15 @@ __device__ __forceinline__ bool bar_wait_fast(uint32_t bar, uint32_t parity) {
   return bar_try(bar, parity) || bar_wait(bar, parity);
 }
 
-// Warp-wide float maximum in one instruction (sm_100 family).
+// Warp-wide float maximum / minimum in one instruction (sm_100 family).
 __device__ __forceinline__ float redux_max(float v) {
   float r;
   asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float redux_min(float v) {
+  float r;
+  asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
 }
 
@@ -436,43 +444,11 @@ __device__ __forceinline__ float warp_kth_largest(float v, int k) {
   return redux_max(v);
 }
 
-// Thread maxima each warp contributes to the chunk threshold: the largest P of
-// its 32 (distinct threads), so the KMAX-th largest of the 8 * P collected
-// values has at least KMAX distinct chunk elements at or above it.  P = 2 for
-// k <= 8 and 4 for k <= 16 keep the expected number of candidates per chunk
-// near k (about 9 for k = 8 on Gaussian logits) and far below kSCand.
-template <int KMAX> constexpr int tau_per_warp() { return KMAX == 1 ? 1 : (KMAX <= 8 ? 2 : 4); }
-
-// Chunk max and top-k threshold from the NV = NW * P collected thread maxima
-// (s_top, 16-byte aligned): every lane reads them all with broadcast loads,
-// lane l < NV ranks value l by (value desc, slot asc), and tau is the value of
-// rank KMAX - 1.  Independent compares instead of a chain of warp reductions.
-template <int NV, int KMAX>
-__device__ __forceinline__ void chunk_max_tau(const float* s_top, float& M, float& tau) {
-  static_assert(NV % 4 == 0 && NV <= 32, "threshold values: a multiple of 4, one warp");
-  const int lane = threadIdx.x & 31;
-  float t[NV];
-#pragma unroll
-  for (int q = 0; q < NV / 4; ++q) {
-    const float4 w = reinterpret_cast<const float4*>(s_top)[q];
-    t[4 * q] = w.x; t[4 * q + 1] = w.y; t[4 * q + 2] = w.z; t[4 * q + 3] = w.w;
-  }
-  float m = t[0];
-#pragma unroll
-  for (int q = 1; q < NV; ++q) m = fmaxf(m, t[q]);
-  M = m;
-  if (KMAX == 1) {
-    tau = m;
-    return;
-  }
-  const int l = lane < NV ? lane : 0;
-  const float mine = s_top[l];
-  int rank = 0;
-#pragma unroll
-  for (int q = 0; q < NV; ++q) rank += (t[q] > mine) | ((t[q] == mine) & (q < l));
-  const unsigned sel = __ballot_sync(0xffffffffu, lane < NV && rank == KMAX - 1);
-  tau = __shfl_sync(0xffffffffu, mine, __ffs(sel) - 1);
-}
+// Chunk threshold: each of the 8 warps contributes its largest thread maximum
+// (k <= 8), or its two largest from distinct threads (k <= 16), and tau is
+// the smallest contribution.  At least 8 (16) distinct elements of the chunk
+// are >= tau, so every member of its top-k is.  One min-reduction, no ranking.
+template <int KMAX> constexpr int tau_per_warp() { return KMAX <= 8 ? 1 : 2; }
 
 __device__ __forceinline__ void bar_named(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -501,10 +477,10 @@ constexpr size_t kStreamHdrBytes = 256;
 // (row, chunk) items from a global counter, so SMs that run slower simply
 // take fewer items, and copies each into the next free ring slot; compute
 // warps never wait on its memory round trips.  Per item the compute warps
-// take thread maxima (bf16 pairs at a time), each warp's top P thread
-// maxima, one named barrier, then the chunk max and threshold tau (k-th
-// largest of the 8 P values: at least k distinct elements are >= tau) and
-// the candidates >= tau, reread from the slot.  After the barrier of item i
+// take thread maxima (bf16 pairs at a time), each warp's largest (k <= 8)
+// or two largest (k <= 16) thread maxima, one named barrier, then the chunk
+// max and the threshold tau (smallest contribution) and the candidates
+// >= tau, reread from the slot.  After the barrier of item i
 // thread 0 frees the slot of item i - 1 and closes that item's record (its
 // candidates are final there).
 constexpr int kStreamThreads = kVThreads + 32;
@@ -519,6 +495,7 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
   constexpr int NW = kVThreads / 32;
   constexpr int P = tau_per_warp<KMAX>();
   constexpr int NV = NW * P;
+  static_assert(NV <= 32, "threshold values must fit one warp");
   constexpr int S = stream_stages<T>();
   constexpr int kSChunkBytes = stream_chunk_bytes<T>();
   extern __shared__ __align__(128) uint8_t ring[];
@@ -582,8 +559,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
     const uint8_t* st = ring + s * kSChunkBytes;
     float my_max;
     float v[EPT];
+    __nv_bfloat162 pm[4];   // packed max of each of this thread's 16-byte vectors
     if (sizeof(T) == 2 && !LSE && n_valid == CH) {
-      __nv_bfloat162 pm[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
@@ -643,8 +620,9 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
       }
     }
     if (item < 0) return;
-    float M, tau;
-    chunk_max_tau<NV, KMAX>(s_top[b], M, tau);
+    const float tv = lane < NV ? s_top[b][lane] : -INFINITY;
+    const float M = redux_max(tv);
+    const float tau = KMAX == 1 ? M : redux_min(lane < NV ? tv : INFINITY);
     if (tid == 0) {
       float ssum = 0.f;
       if constexpr (LSE) {
@@ -668,11 +646,13 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
         }
       };
       if (sizeof(T) == 2 && !LSE && n_valid == CH) {
-        // reread this thread's values (the slot is freed at the next barrier);
-        // tau is one of the chunk's elements, so exact in bf16
+        // reread only the vectors whose maximum reaches tau (the slot is freed
+        // at the next barrier); tau is one of the chunk's elements, so exact
+        // in bf16
         const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          if (!__hge2_mask(pm[j], t2)) continue;
           const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -694,9 +674,10 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
   }
 }
 
-// One warp per row.  The warp reads the row's chunk headers (max, sum,
-// candidate count, overflow) with one 16-byte load per lane and takes the
-// row max and sum.  Row threshold: the KMAX-th largest chunk maximum; KMAX
+// One warp per row.  In one round trip the warp reads every chunk header
+// (max, sum, candidate count, overflow; one 16-byte load per lane) and the
+// first 32 entries of every chunk's candidate list, and takes the row max
+// and sum.  Row threshold: the KMAX-th largest chunk maximum; KMAX
 // distinct elements reach it, so every member of the row's top-k is >= it,
 // and only chunks whose maximum reaches it (about KMAX of them) are opened.
 // Their candidates >= the threshold (a chunk that overflowed is rescanned
@@ -726,7 +707,7 @@ __device__ __forceinline__ void warp_bitonic_desc(float& v, int& i) {
 }
 
 template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
+__global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel(
     const StreamPart* __restrict__ part, int n_chunks, int rows, const T* __restrict__ logits, int V,
     int64_t ld, const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_val, float* __restrict__ row_max,
@@ -751,17 +732,38 @@ __global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
   };
 
   if (n_chunks <= 32) {
+    // one round trip: every chunk's header (lane c) and the first 32 entries
+    // of every chunk's candidate list (lane l: entry l of each) at once
     float mc = -INFINITY, sc = 0.f;
     int cc = 0, oc = 0;
     if (lane < n_chunks) {
-      const uint4 h = *reinterpret_cast<const uint4*>(gp + lane);
+      const uint4 h = __ldcg(reinterpret_cast<const uint4*>(gp + lane));
       mc = __uint_as_float(h.x); sc = __uint_as_float(h.y);
       cc = static_cast<int>(h.z); oc = static_cast<int>(h.w);
+    }
+    float cv[32];
+    int ci[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      cv[c] = -INFINITY;
+      ci[c] = INT32_MAX;
+      if (c < n_chunks) { cv[c] = __ldcg(&gp[c].val[lane]); ci[c] = __ldcg(&gp[c].idx[lane]); }
     }
     const float M = redux_max(mc);
     float S = 0.f;
     if (LSE) S = warp_sum(mc != -INFINITY ? sc * ex2((mc - M) * kLog2e) : 0.f);
-    const float tau = KMAX == 1 ? M : (n_chunks >= KMAX ? warp_kth_largest(mc, KMAX) : -INFINITY);
+    // rank of each chunk maximum (value desc, chunk asc); tau = rank KMAX - 1
+    float tau = M;
+    if (KMAX > 1) {
+      int rank = 0;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float o = __shfl_sync(0xffffffffu, mc, c);
+        rank += c < n_chunks && (o > mc || (o == mc && c < lane));
+      }
+      const unsigned sel = __ballot_sync(0xffffffffu, lane < n_chunks && rank == KMAX - 1);
+      tau = sel ? __shfl_sync(0xffffffffu, mc, __ffs(sel) - 1) : -INFINITY;   // fewer chunks than KMAX
+    }
     const unsigned surv = __ballot_sync(0xffffffffu, lane < n_chunks && mc >= tau);
     const unsigned ovfm = __ballot_sync(0xffffffffu, oc != 0);
     int nb = 0;   // buffered candidates, warp-uniform
@@ -771,28 +773,23 @@ __global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
       if (keep && pos < kMergeBuf) { s_bv[wl][pos] = v; s_bi[wl][pos] = e; }
       nb += __popc(bal);
     };
-    // stored candidates of the opened chunks, four chunks' loads in flight
-    unsigned todo = surv & ~ovfm;
-    while (todo) {
-      int cs[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        cs[u] = todo ? __ffs(todo) - 1 : -1;
-        todo &= todo - 1u;
+    for (int c = 0; c < 32; ++c) {
+      if (!((surv & ~ovfm) >> c & 1u)) continue;
+      const int n = __shfl_sync(0xffffffffu, cc, c);
+      append(lane < n && cv[c] >= tau, cv[c], ci[c]);
+    }
+    // rare: opened lists longer than one warp's worth
+    for (unsigned todo = surv & ~ovfm; todo; todo &= todo - 1u) {
+      const int c = __ffs(todo) - 1;
+      const int n = __shfl_sync(0xffffffffu, cc, c);
+      for (int q0 = 32; q0 < n; q0 += 32) {
+        const int q = q0 + lane;
+        const bool in = q < n;
+        const float x = in ? __ldcg(&gp[c].val[q]) : -INFINITY;
+        const int e = in ? __ldcg(&gp[c].idx[q]) : INT32_MAX;
+        append(in && x >= tau, x, e);
       }
-      float vv[4];
-      int ii[4];
-      bool kk[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int n = __shfl_sync(0xffffffffu, cc, cs[u] & 31);
-        kk[u] = cs[u] >= 0 && lane < n;
-        vv[u] = -INFINITY;
-        ii[u] = INT32_MAX;
-        if (kk[u]) { vv[u] = gp[cs[u]].val[lane]; ii[u] = gp[cs[u]].idx[lane]; }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) append(kk[u] && vv[u] >= tau, vv[u], ii[u]);
     }
     // opened chunks whose candidate list overflowed: rescan their logits
     unsigned rescan = surv & ovfm;
@@ -858,7 +855,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
   for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
   for (int c = 0; c < n_chunks; ++c) {
     if (!gp[c].ovf) {
-      if (lane < gp[c].cnt) list_insert<KMAX>(lv, li, gp[c].val[lane], gp[c].idx[lane]);
+      const int n = gp[c].cnt;
+      for (int q = lane; q < n; q += 32) list_insert<KMAX>(lv, li, gp[c].val[q], gp[c].idx[q]);
     } else {
       const int e1 = min(V, (c + 1) * kVChunk);
       for (int e = c * kVChunk + lane; e < e1; e += 32) list_insert<KMAX>(lv, li, logit(e), e);
@@ -981,7 +979,7 @@ TV_API int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = size_t(8) << 20;   // TV_NOALLOC_SCRATCH_BYTES
+constexpr size_t kNoallocScratchBytes = size_t(32) << 20;   // TV_NOALLOC_SCRATCH_BYTES
 constexpr int kNoallocMaxDevices = 64;
 
 // Loaded with the library on every GPU that uses it and kept until exit.
