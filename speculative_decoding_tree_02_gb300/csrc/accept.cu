@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(1024) accept_kernel(
   __shared__ int s_warp_best[32];
   __shared__ int s_best;
 
+  griddep_wait();
+  griddep_release();
   const int r = blockIdx.x;
   const int n0 = node_off[r];
   const int N = min(node_off[r + 1] - n0, TV_MAX_NODES);
@@ -91,8 +93,7 @@ TV_API int accept_longest_path(const int32_t* parent, const int32_t* tok, const 
     return TV_EINVAL;
   if (B > (1 << 30)) return TV_EUNSUPPORTED;
   const int threads = max(32, (max_nodes + 31) / 32 * 32);
-  tv::accept_kernel<<<B, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      parent, tok, argmax, valid, node_off, max_depth, accept_len, best_node, path, bonus,
-      path_acc);
-  return tv::launch_status();
+  return tv::launch_pdl(tv::accept_kernel, dim3(B), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                        parent, tok, argmax, valid, node_off, max_depth, accept_len, best_node, path, bonus,
+                        path_acc);
 }

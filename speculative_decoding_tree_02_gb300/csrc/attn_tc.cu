@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
   const uint32_t sb = smem_u32(sm);
   const AttnParams& p = P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_release();
   const int kvh = blockIdx.x, tile = blockIdx.y;
   const int4 unit = p.plan[blockIdx.z];
   const int r = unit.x;
@@ -695,6 +697,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* 
                                                                  int* __restrict__ status) {
   __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets], s_w[33];
   __shared__ int s_base;
+  griddep_wait();
+  griddep_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) { *status = 0; s_base = 0; }
   for (int i = tid; i < n_cnt; i += kPlanThreads) piece_cnt[i] = 0;
@@ -860,11 +864,10 @@ static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long 
   }
   if (!ok) return TV_ECUDA;
   const int tiles = (p.max_nodes + nq - 1) / nq;
-  tc::attn_plan_kernel<<<1, tc::kPlanThreads, 0, st>>>(p.pre_off, p.B, p.piece_len, p.n_units / p.B, p.n_units,
-                                                       const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles, err);
-  dim3 grid(p.Hkv, tiles, p.n_units);
-  tc::attn_tc_kernel<LIVE><<<grid, L::kThreads, L::kSmemBytes, st>>>(P);
-  return launch_status();
+  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st, p.pre_off, p.B, p.piece_len,
+                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles, err);
+  if (rc != TV_OK) return rc;
+  return launch_pdl(tc::attn_tc_kernel<LIVE>, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
 }
 
 int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st) {

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
   extern __shared__ unsigned long long s_key[];                       // [n] sort keys
   int* s_rank = reinterpret_cast<int*>(s_key + kDcutMaxPos);          // [T]
   __shared__ uint4 s_w[33];
+  griddep_wait();
+  griddep_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = D + 1;
   const int T = B * N;
@@ -251,9 +253,8 @@ TV_API int dcut_select(const float* conf, int B, int D, const float* rho, int n_
   if (!attr) return TV_ECUDA;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const int Ti = static_cast<int>(T);
-  if (Ti <= 1024) tv::dcut_kernel<1><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
-  else if (Ti <= 2048) tv::dcut_kernel<2><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
-  else if (Ti <= 4096) tv::dcut_kernel<4><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
-  else tv::dcut_kernel<8><<<1, tv::kDcutThreads, bytes, st>>>(conf, B, D, n_rho, ks, score, keep, keep_len, pack_off, pack_idx);
-  return tv::launch_status();
+  auto kern = Ti <= 1024 ? tv::dcut_kernel<1> : Ti <= 2048 ? tv::dcut_kernel<2> : Ti <= 4096 ? tv::dcut_kernel<4>
+                                                                                  : tv::dcut_kernel<8>;
+  return tv::launch_pdl(kern, dim3(1), dim3(tv::kDcutThreads), bytes, st, conf, B, D, n_rho, ks, score, keep,
+                        keep_len, pack_off, pack_idx);
 }

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kAdjWarps * 32) adj_update_kernel(
     int32_t* __restrict__ n_bad, bool vec4) {
   extern __shared__ int32_t s_win[];   // [kAdjWarps][kAdjRows]
   __shared__ int s_bad[kAdjWarps];
+  griddep_wait();
+  griddep_release();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * kAdjRows;
   int32_t* my = s_win + warp * kAdjRows;
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(128) retrieve_kernel(
     const int32_t* __restrict__ trank, const int32_t* __restrict__ tmpl_off, int n_stage,
     int max_slots, int32_t* __restrict__ rtok, int32_t* __restrict__ rparent,
     int32_t* __restrict__ nslots, int32_t* __restrict__ err) {
+  griddep_wait();
+  griddep_release();
   const int b = blockIdx.y;
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B || s >= max_slots) return;
@@ -155,9 +159,9 @@ TV_API int graft_adj_update(int32_t* adj, int V, int k, const int32_t* tok,
   // rows and top-k records start on 16-byte boundaries: copy 4 ints at a time
   const bool vec4 = (k % 4 == 0) && (topk_ld % 4 == 0) && tv::aligned(adj, 16) &&
                     tv::aligned(topk_idx, 16);
-  tv::adj_update_kernel<<<grid, tv::kAdjWarps * 32, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      adj, V, k, tok, topk_idx, topk_ld, valid, n, n_bad, vec4);
-  return tv::launch_status();
+  return tv::launch_pdl(tv::adj_update_kernel, dim3(grid), dim3(tv::kAdjWarps * 32), smem,
+                        reinterpret_cast<cudaStream_t>(stream), adj, V, k, tok, topk_idx, topk_ld, valid, n, n_bad,
+                        vec4);
 }
 
 TV_API int graft_retrieve(const int32_t* adj, int V, int k, const int32_t* root_tok,
@@ -171,8 +175,7 @@ TV_API int graft_retrieve(const int32_t* adj, int V, int k, const int32_t* root_
   if (!tparent || !trank) return TV_EINVAL;
   if (B > 65535) return TV_EUNSUPPORTED;
   dim3 grid((max_slots + 127) / 128, B);
-  tv::retrieve_kernel<<<grid, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      adj, V, k, root_tok, stage, B, tparent, trank, tmpl_off, n_stage, max_slots, rtok, rparent,
-      nslots, err);
-  return tv::launch_status();
+  return tv::launch_pdl(tv::retrieve_kernel, grid, dim3(128), 0, reinterpret_cast<cudaStream_t>(stream), adj, V, k,
+                        root_tok, stage, B, tparent, trank, tmpl_off, n_stage, max_slots, rtok, rparent, nslots,
+                        err);
 }

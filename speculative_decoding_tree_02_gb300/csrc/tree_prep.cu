@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) tree_prep_kernel(
     const int32_t* __restrict__ prefix_len, const int32_t* __restrict__ vis_prefix, int W,
     int32_t* __restrict__ depth, int32_t* __restrict__ pos, uint64_t* __restrict__ anc,
     int32_t* __restrict__ vis_out, int32_t* __restrict__ err) {
+  griddep_wait();
+  griddep_release();
   const int r = blockIdx.y;
   const int n0 = node_off[r];
   const int N = node_off[r + 1] - n0;
@@ -67,7 +69,6 @@ TV_API int tv_tree_prep(const int32_t* parent, const int32_t* node_off, const in
   if (B > 65535) return TV_EUNSUPPORTED;
   const int per_req = max_nodes * anc_words;
   dim3 grid((per_req + 255) / 256, B);
-  tv::tree_prep_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      parent, node_off, prefix_len, vis_prefix, anc_words, depth, pos, anc, vis_out, err);
-  return tv::launch_status();
+  return tv::launch_pdl(tv::tree_prep_kernel, grid, dim3(256), 0, reinterpret_cast<cudaStream_t>(stream), parent,
+                        node_off, prefix_len, vis_prefix, anc_words, depth, pos, anc, vis_out, err);
 }

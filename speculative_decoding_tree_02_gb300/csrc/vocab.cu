@@ -473,6 +473,13 @@ struct StreamHdr {
 };
 constexpr size_t kStreamHdrBytes = 256;
 
+__global__ void stream_hdr_clear_kernel(StreamHdr* hdr) {
+  griddep_wait();
+  griddep_release();
+  hdr->status = 0;
+  hdr->claim = 0;
+}
+
 // CTA = 8 compute warps + 1 producer warp.  The producer's lane 0 claims
 // (row, chunk) items from a global counter, so SMs that run slower simply
 // take fewer items, and copies each into the next free ring slot; compute
@@ -507,6 +514,8 @@ __global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
+  griddep_wait();
+  griddep_release();
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
@@ -714,6 +723,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel
     float* __restrict__ row_lse) {
   __shared__ float s_bv[kMergeWarps][kMergeBuf];
   __shared__ int s_bi[kMergeWarps][kMergeBuf];
+  griddep_wait();
+  griddep_release();
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int row = blockIdx.x * kMergeWarps + wl;
   if (row >= rows) return;
@@ -907,12 +918,15 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
     const int grid = std::min(items, 3 * sm_count_cached());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
     auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
-    if (cudaMemsetAsync(hdr, 0, sizeof(StreamHdr), st) != cudaSuccess) return TV_ECUDA;
-    vocab_stream_kernel<T, KMAX, LSE><<<grid, kStreamThreads, smem, st>>>(logits, V, ld, row_idx, rows, n_chunks,
-                                                                           sp, hdr);
-    vocab_stream_merge_kernel<T, KMAX, LSE><<<(rows + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
-        sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax, topk_idx, topk_val, row_max, row_lse);
-    return launch_status();
+    int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr);
+    if (rc == TV_OK)
+      rc = launch_pdl(vocab_stream_kernel<T, KMAX, LSE>, dim3(grid), dim3(kStreamThreads), smem, st, logits, V, ld,
+                      row_idx, rows, n_chunks, sp, hdr);
+    if (rc == TV_OK)
+      rc = launch_pdl(vocab_stream_merge_kernel<T, KMAX, LSE>, dim3((rows + kMergeWarps - 1) / kMergeWarps),
+                      dim3(32 * kMergeWarps), 0, st, sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax,
+                      topk_idx, topk_val, row_max, row_lse);
+    return rc;
   }
   dim3 g1(n_chunks, rows);
   vocab_partial_kernel<T, KMAX, LSE><<<g1, kVThreads, 0, st>>>(logits, V, ld, row_idx, vec_ok, part);
