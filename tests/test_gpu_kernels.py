@@ -181,6 +181,14 @@ def test_alpha_small_forest(tv):
     check_alpha(tv, d)
 
 
+@pytest.mark.parametrize("V", [40, 1001, 4104])
+def test_alpha_small_and_ragged_vocab(tv, V):
+    # V = 40: five of the eight slices of the one-read path are empty;
+    # V = 1001: rows not a multiple of 8 elements take the two-pass path
+    d = synth.specopd_tree(prompt=16, response=48, n_anchor=4, W=3, V=V, with_attention=False)
+    check_alpha(tv, d)
+
+
 def test_alpha_identity_is_one(tv):
     d = synth.specopd_tree(prompt=8, response=24, n_anchor=3, W=4, V=151936, with_attention=False)
     d["lq"] = d["lp"].copy()
