@@ -366,7 +366,10 @@ def measure_rows(tv, torch, pk, stream):
              torch.randperm(V, device="cuda", generator=g).to(torch.int32),
              torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32)) for _ in range(nc)]
     nb = torch.zeros(1, dtype=torch.int32, device="cuda")
-    grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb), stream) for a, t, k in sets]
+    wsa = torch.empty(max(256, tv.load_library().graft_adj_update_workspace_size(V, V)), dtype=torch.uint8,
+                      device="cuda")
+    grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb, ws=wsa), stream)
+           for a, t, k in sets]
     rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
         time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
     return rows

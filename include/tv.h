@@ -240,7 +240,11 @@ int accept_longest_path(const int32_t* parent, const int32_t* tok, const int32_t
  * Graft page §2 (second/third gear) and §6: after verification, every
  * verified position, accepted or rejected, rewrites the row of its token with
  * the target's top-k next tokens.  Several nodes with the same token: the
- * last in index order wins; rows are overwritten, never merged.  Atomics-free.
+ * last in index order wins; rows are overwritten, never merged.  The result
+ * does not depend on scheduling: up to TV_ADJ_SCAN_MAX nodes an ordered scan
+ * per table slice picks each row's last node; larger batches (a whole-table
+ * refresh) record each token's last node with an integer maximum in the
+ * workspace, then copy once per row.
  *
  *   adj       int32 [V, k], updated in place
  *   tok       int32 [n] tokens of the verified nodes
@@ -248,9 +252,14 @@ int accept_longest_path(const int32_t* parent, const int32_t* tok, const int32_t
  *   valid     uint8 [n] or NULL: nodes with valid == 0 are skipped
  *   n_bad     int32 (device, may be NULL): receives the number of valid nodes
  *             whose token lies outside [0, V) (those are skipped)
+ *   ws        graft_adj_update_workspace_size(V, n) bytes (0 when n <=
+ *             TV_ADJ_SCAN_MAX: ws may then be NULL), 16-byte aligned
  * -------------------------------------------------------------------------- */
+#define TV_ADJ_SCAN_MAX 4096
+size_t graft_adj_update_workspace_size(int V, int n);
 int graft_adj_update(int32_t* adj, int V, int k, const int32_t* tok, const int32_t* topk_idx,
-                     int topk_ld, const uint8_t* valid, int n, int32_t* n_bad, tv_stream_t stream);
+                     int topk_ld, const uint8_t* valid, int n, int32_t* n_bad, void* ws,
+                     size_t ws_bytes, tv_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * graft_retrieve — expand retrieval candidates from the successor table by a

@@ -43,7 +43,8 @@ _SIGS = {
     "tree_tv_alpha_workspace_size": (_SZ, [_I, _I]),
     "tree_tv_alpha": (_I, [_P, _P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "accept_longest_path": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-    "graft_adj_update": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _P, _P]),
+    "graft_adj_update_workspace_size": (_SZ, [_I, _I]),
+    "graft_adj_update": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _P]),
     "graft_retrieve": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dcut_select_workspace_size": (_SZ, [_I, _I, _I]),
     "dcut_select": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -252,13 +253,17 @@ def accept_longest_path(parent, tok, argmax, node_off, valid=None, max_nodes=Non
 
 
 # -------------------------------------------------------------------------- Graft
-def graft_adj_update(adj, tok, topk_idx, valid=None, n_bad=None):
+def graft_adj_update(adj, tok, topk_idx, valid=None, n_bad=None, ws=None):
     V, k = adj.shape
     n = tok.numel()
     if n_bad is None:
         n_bad = torch.zeros(1, dtype=torch.int32, device=adj.device)
+    need = load_library().graft_adj_update_workspace_size(V, n)
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=adj.device)
     _check("graft_adj_update", load_library().graft_adj_update(
-        _ptr(adj), V, k, _ptr(tok), _ptr(topk_idx), topk_idx.stride(0), _ptr(valid), n, _ptr(n_bad), _stream()))
+        _ptr(adj), V, k, _ptr(tok), _ptr(topk_idx), topk_idx.stride(0), _ptr(valid), n, _ptr(n_bad),
+        _ptr(ws) if need else None, ws.numel() if need else 0, _stream()))
     return n_bad
 
 

@@ -6,9 +6,9 @@
 namespace tv {
 
 // ---------------------------------------------------------------------------
-// graft_adj_update — atomics-free, deterministic "last writer wins".
+// graft_adj_update — deterministic "last writer wins".
 //
-// CTA b owns table rows [b*R, b*R + R).  Its 32 warps split the node list into
+// Up to TV_ADJ_SCAN_MAX nodes (a verification step): CTA b owns table rows [b*R, b*R + R).  Its 32 warps split the node list into
 // 32 contiguous, ordered segments.  A warp walks its segment 32 nodes at a
 // time; lanes whose tokens fall in the CTA's rows group equal tokens with
 // __match_any_sync and only the highest lane (the latest node) records its
@@ -71,6 +71,56 @@ __global__ void __launch_bounds__(kAdjWarps * 32) adj_update_kernel(
   if (win < 0) return;
   const int32_t* src = topk + static_cast<int64_t>(win) * topk_ld;
   int32_t* dst = adj + static_cast<int64_t>(t0 + row) * k;
+  if (vec4) {
+    for (int c = 0; c < k; c += 4)
+      *reinterpret_cast<int4*>(dst + c) = *reinterpret_cast<const int4*>(src + c);
+  } else {
+    for (int c = 0; c < k; ++c) dst[c] = src[c];
+  }
+}
+
+// Large batches (n > TV_ADJ_SCAN_MAX, e.g. a whole-table refresh): the scan
+// above would read the node list once per table slice.  Instead: last[t] =
+// largest valid node index with token t (integer atomicMax: the same result
+// in any order), then one thread per row copies the winner's top-k.
+__global__ void __launch_bounds__(256) adj_last_init_kernel(int32_t* __restrict__ last, int V,
+                                                            int32_t* __restrict__ n_bad) {
+  griddep_wait();
+  griddep_release();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < V) last[t] = -1;
+  if (t == 0 && n_bad) *n_bad = 0;
+}
+
+__global__ void __launch_bounds__(256) adj_last_kernel(int32_t* __restrict__ last, int V,
+                                                       const int32_t* __restrict__ tok,
+                                                       const uint8_t* __restrict__ valid, int n,
+                                                       int32_t* __restrict__ n_bad) {
+  griddep_wait();
+  griddep_release();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  bool bad = false;
+  if (i < n && (!valid || valid[i])) {
+    const int t = tok[i];
+    if (t < 0 || t >= V) bad = true;
+    else atomicMax(&last[t], i);
+  }
+  const unsigned b = __ballot_sync(0xffffffffu, bad);
+  if (b && (threadIdx.x & 31) == 0 && n_bad) atomicAdd(n_bad, __popc(b));
+}
+
+__global__ void __launch_bounds__(256) adj_copy_kernel(int32_t* __restrict__ adj, int V, int k,
+                                                       const int32_t* __restrict__ last,
+                                                       const int32_t* __restrict__ topk, int topk_ld,
+                                                       bool vec4) {
+  griddep_wait();
+  griddep_release();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= V) return;
+  const int win = last[t];
+  if (win < 0) return;
+  const int32_t* src = topk + static_cast<int64_t>(win) * topk_ld;
+  int32_t* dst = adj + static_cast<int64_t>(t) * k;
   if (vec4) {
     for (int c = 0; c < k; c += 4)
       *reinterpret_cast<int4*>(dst + c) = *reinterpret_cast<const int4*>(src + c);
@@ -143,25 +193,40 @@ __global__ void __launch_bounds__(128) retrieve_kernel(
 
 }  // namespace tv
 
+TV_API size_t graft_adj_update_workspace_size(int V, int n) {
+  if (V <= 0 || n <= TV_ADJ_SCAN_MAX) return 0;
+  return (static_cast<size_t>(V) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+}
+
 TV_API int graft_adj_update(int32_t* adj, int V, int k, const int32_t* tok,
                             const int32_t* topk_idx, int topk_ld, const uint8_t* valid, int n,
-                            int32_t* n_bad, tv_stream_t stream) {
+                            int32_t* n_bad, void* ws, size_t ws_bytes, tv_stream_t stream) {
   if (V <= 0 || k <= 0 || n < 0 || topk_ld < k) return TV_EINVAL;
   if (k > TV_MAX_TOPK) return TV_EUNSUPPORTED;
   if (n == 0) return TV_OK;
   if (!adj || !tok || !topk_idx) return TV_EINVAL;
+  // rows and top-k records start on 16-byte boundaries: copy 4 ints at a time
+  const bool vec4 = (k % 4 == 0) && (topk_ld % 4 == 0) && tv::aligned(adj, 16) &&
+                    tv::aligned(topk_idx, 16);
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  if (n > TV_ADJ_SCAN_MAX) {
+    if (!ws || ws_bytes < graft_adj_update_workspace_size(V, n) || !tv::aligned(ws, 16)) return TV_EWORKSPACE;
+    auto* last = static_cast<int32_t*>(ws);
+    const int gv = (V + 255) / 256, gn = (n + 255) / 256;
+    int rc = tv::launch_pdl(tv::adj_last_init_kernel, dim3(gv), dim3(256), 0, st, last, V, n_bad);
+    if (rc == TV_OK) rc = tv::launch_pdl(tv::adj_last_kernel, dim3(gn), dim3(256), 0, st, last, V, tok, valid, n, n_bad);
+    if (rc == TV_OK)
+      rc = tv::launch_pdl(tv::adj_copy_kernel, dim3(gv), dim3(256), 0, st, adj, V, k, last, topk_idx, topk_ld, vec4);
+    return rc;
+  }
   static const int smem = [] {
     const int bytes = tv::kAdjWarps * tv::kAdjRows * static_cast<int>(sizeof(int32_t));
     cudaFuncSetAttribute(tv::adj_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return bytes;
   }();
   const int grid = (V + tv::kAdjRows - 1) / tv::kAdjRows;
-  // rows and top-k records start on 16-byte boundaries: copy 4 ints at a time
-  const bool vec4 = (k % 4 == 0) && (topk_ld % 4 == 0) && tv::aligned(adj, 16) &&
-                    tv::aligned(topk_idx, 16);
-  return tv::launch_pdl(tv::adj_update_kernel, dim3(grid), dim3(tv::kAdjWarps * 32), smem,
-                        reinterpret_cast<cudaStream_t>(stream), adj, V, k, tok, topk_idx, topk_ld, valid, n, n_bad,
-                        vec4);
+  return tv::launch_pdl(tv::adj_update_kernel, dim3(grid), dim3(tv::kAdjWarps * 32), smem, st, adj, V, k, tok,
+                        topk_idx, topk_ld, valid, n, n_bad, vec4);
 }
 
 TV_API int graft_retrieve(const int32_t* adj, int V, int k, const int32_t* root_tok,

@@ -254,11 +254,11 @@ def test_accept_chain_1024_and_truncated_path(tv):
 
 
 # ------------------------------------------------------------------ Graft table
-def test_adj_update_duplicates_invalid_and_bad_tokens(tv):
+@pytest.mark.parametrize("n", [3000, 5000])   # ordered scan / last-index table
+def test_adj_update_duplicates_invalid_and_bad_tokens(tv, n):
     rng = np.random.default_rng(1)
     V, k = 3000, 8
     adj = rng.integers(0, V, (V, k)).astype(np.int32)
-    n = 5000
     tok = rng.integers(0, 400, n).astype(np.int32)        # many duplicates
     tok[::97] = V + 3                                       # out of range
     tok[5::101] = -2
