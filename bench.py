@@ -372,7 +372,53 @@ def measure_rows(tv, torch, pk, stream):
            for a, t, k in sets]
     rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
         time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
+    del sets, grs
+    # a2 on the large-tree shapes, against the bf16 tensor peak: the SpecOPD
+    # proposal tree (1024 nodes over one 4096-token trunk, 64 anchors) and the
+    # BlockPilot sweep (8 requests x 8192-token prefix x 113 nodes)
+    for name, d in (("specopd 1024 nodes, trunk 4096", synth.specopd_tree(with_logits=False)),
+                    ("blockpilot 8x(8192 prefix + 113 nodes)", synth.blockpilot_sweep(with_mlp=False, V=64))):
+        rows[f"tree_verify_attn[{name}]"] = large_tree_row(tv, torch, d, pk, stream)
     return rows
+
+
+def large_tree_row(tv, torch, d, pk, stream):
+    """Attention on one large-tree workload: algorithmic flops = 4·d per
+    (query head, node, visible key), visible keys = the node's visible prefix
+    plus its ancestors (itself included)."""
+    off, pre_off = d["node_off"], d["pre_off"]
+    sizes, plen = np.diff(off), np.diff(pre_off).astype(np.int32)
+    max_nodes, max_prefix = int(sizes.max()), int(plen.max())
+    parent = d["parent"]
+    depth = np.zeros(parent.size, np.int64)
+    for i, p in enumerate(parent):          # parents precede children within a request
+        if p >= 0:
+            depth[i] = depth[off[np.searchsorted(off, i, side="right") - 1] + p] + 1
+    vis = d["vis_prefix"] if d.get("vis_prefix") is not None else np.repeat(plen, sizes)
+    n, Hq, dd = d["q"].shape
+    Hkv = d["k_tree"].shape[1]
+    flops = 4 * dd * Hq * int((vis.astype(np.int64) + depth + 1).sum())
+    # bytes: each request's visible prefix K/V once per KV head, q, o, tree K/V
+    kv_pre = sum(int(vis[off[r]:off[r + 1]].max()) for r in range(len(sizes))) * Hkv * dd * 2 * 2
+    byts = kv_pre + n * (2 * Hq * dd * 2 + 2 * Hkv * dd * 2)
+    one = sum(d[k].nbytes for k in ("q", "k_pre", "v_pre", "k_tree", "v_tree")) + d["q"].nbytes
+    sets = []
+    for _ in range(copies_for(one)):
+        t = {k: to_dev(d[k], torch) for k in ("q", "k_pre", "v_pre", "k_tree", "v_tree")}
+        t["out"] = torch.empty_like(t["q"])
+        sets.append(t)
+    dv = {k: to_dev(v, torch) for k, v in (("off", off), ("pre_off", pre_off), ("plen", plen),
+                                            ("parent", parent), ("vis", vis.astype(np.int32)))}
+    anc = tv.tv_tree_prep(dv["parent"], dv["off"], dv["plen"], dv["vis"], max_nodes, (max_nodes + 63) // 64)[2]
+    ws = torch.empty(max(256, tv.load_library().tree_verify_attn_workspace_size(
+        len(sizes), max_nodes, max_prefix, Hq, Hkv, dd, 1)), dtype=torch.uint8, device="cuda")
+    grs = [capture(torch, lambda t=t: tv.tree_verify_attn(
+        t["q"], t["k_pre"], t["v_pre"], dv["pre_off"], t["k_tree"], t["v_tree"], dv["off"], anc, max_nodes,
+        max_prefix, vis_prefix=dv["vis"], out=t["out"], want_lse=False, ws=ws), stream) for t in sets]
+    us = time_graph(torch, grs, 10 * len(sets), stream) * 1e3
+    tfl = flops / us / 1e6
+    return {"us": round(us, 2), "flops": flops, "tflops": round(tfl, 1), "frac": round(tfl / pk["bf16"], 3),
+            "bound": "tensor", "bytes": byts, "gbs": round(byts / us / 1e3, 1)}
 
 
 def gpu_arm(args):
