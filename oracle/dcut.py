@@ -60,3 +60,28 @@ def select(conf, rhos):
         flat = np.nonzero(keep[a].reshape(-1))[0]
         pack_idx[a, :flat.size] = flat
     return s, keep, keep_len, pack_off, pack_idx
+
+
+def expected_tokens(s, keep):
+    """Expected tokens that one verification step yields at each budget: the
+    sum of the kept positions' survival probabilities s (a kept root yields the
+    target's own next token, s = 1).  This is the expected-gain side of the
+    runtime budget choice (D-cut page, technical summary section 2: expected
+    MAT from the confidence estimates), summed over the batch.  Exact sum
+    (math.fsum of the fp32 scores), returned as float64 [n_rho]."""
+    s = np.asarray(s, np.float32)
+    return np.array([math.fsum(float(x) for x in s[keep[a].astype(bool)]) for a in range(keep.shape[0])],
+                    np.float64)
+
+
+def choose_rho(E, cost):
+    """rho* index = argmax over budgets of E[a] / cost[a], the expected gain
+    over the profiled step cost (same section: the ratio of expected MAT to
+    the hardware-profiled run cost); the lowest index on ties.  The cost table
+    is an input (its calibration is out of scope)."""
+    best, arg = -math.inf, -1
+    for a in range(len(E)):
+        v = float(E[a]) / float(cost[a])
+        if v > best:
+            best, arg = v, a
+    return arg

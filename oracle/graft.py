@@ -23,6 +23,25 @@ Readings used here:
     qualitative shape, so the exact slots are *parity unpinned* against the
     pages (the retrieval given a template is pinned).
   * the retrieved subtree hangs off the tree root (the current token).
+
+Next rows built on the same table (readings, the pages give no procedure):
+  * stage decision (section 2, first gear): draft layer L of a node is its
+    depth - 1 (the root is the current token, depth 0); its cumulative
+    confidence is the fp32 product of the drafter confidences on its path,
+    root excluded, in root-to-node order.  At the checkpoints, layers 0, 1
+    and 5, the best (largest) cumulative confidence of the layer is compared
+    with that checkpoint's calibrated threshold; the first checkpoint below
+    its threshold gives the stage 0, 1, 2 (8/52, 24/36, 40/20), none gives 3
+    (60/0).  A layer the draft does not reach counts as best = 0.
+  * batched static-tree replacement (section 4, batched serving): the
+    per-request slot count S stays fixed; draft nodes whose cumulative
+    confidence is below the threshold, and their descendants, are replaced
+    by retrieval nodes: the first S - kept slots of the best-first template,
+    rooted at the current token.  Kept nodes keep their order.
+  * Graft-TAIL (section 7): a block draft is a chain; its confident prefix
+    (cumulative confidence >= threshold) is kept and the tail is replaced by
+    the first retrieval slots of the best-first template, continuing from the
+    last kept token (the deepest kept node).
 """
 from __future__ import annotations
 
@@ -106,3 +125,81 @@ def assemble_hybrid(parent_draft, tparent_stage):
     for p in tparent_stage:
         parent.append(0 if p < 0 else nd + int(p))
     return np.array(parent, np.int32)
+
+
+CHECKPOINT_LAYERS = (0, 1, 5)
+
+
+def cumulative_confidence(parent, conf):
+    """depth int32 [N] (root 0) and cumulative confidence float32 [N]: the
+    fp32 product of conf along the path, root excluded, root-to-node order
+    (root: 1).  Parents precede their children (request-local indices)."""
+    n = len(parent)
+    depth = np.zeros(n, np.int32)
+    c = np.ones(n, np.float32)
+    for i in range(n):
+        p = int(parent[i])
+        if p >= 0:
+            depth[i] = depth[p] + 1
+            c[i] = np.float32(c[p] * np.float32(conf[i]))
+    return depth, c
+
+
+def stage_decision(parent, conf, node_off, tau):
+    """Per request: best cumulative confidence at the checkpoint layers and the
+    stage (first checkpoint whose best value is below its threshold; 3 if
+    none).  Returns stage int32 [B], best float32 [B, 3]."""
+    B = len(node_off) - 1
+    stage = np.full(B, 3, np.int32)
+    best = np.zeros((B, len(CHECKPOINT_LAYERS)), np.float32)
+    for r in range(B):
+        a, b = int(node_off[r]), int(node_off[r + 1])
+        depth, c = cumulative_confidence(parent[a:b], conf[a:b])
+        for j, L in enumerate(CHECKPOINT_LAYERS):
+            at = c[depth == L + 1]
+            best[r, j] = at.max() if at.size else np.float32(0.0)
+        for j in range(len(CHECKPOINT_LAYERS)):
+            if best[r, j] < np.float32(tau[j]):
+                stage[r] = j
+                break
+    return stage, best
+
+
+def graft_replace(parent, tok, conf, node_off, S, tau, attach, adj, tparent_bf, trank_bf):
+    """Static-tree replacement (attach = 0: retrieval rooted at the current
+    token) and Graft-TAIL (attach = 1: rooted at the deepest kept node, ties:
+    larger cumulative confidence, then lower index).  Request r has S nodes
+    (node 0 its root).  Returns tok_out, parent_out int32 [B, S] (-1 padded),
+    n_kept int32 [B]; retrieval slot s follows the best-first template
+    (tparent_bf, trank_bf), its first S - n_kept entries."""
+    B = len(node_off) - 1
+    tok_out = np.full((B, S), -1, np.int32)
+    par_out = np.full((B, S), -1, np.int32)
+    n_kept = np.zeros(B, np.int32)
+    for r in range(B):
+        a = int(node_off[r])
+        p_loc = [int(x) for x in parent[a:a + S]]
+        depth, c = cumulative_confidence(p_loc, conf[a:a + S])
+        keep = [False] * S
+        for i in range(S):
+            keep[i] = i == 0 or (c[i] >= np.float32(tau) and keep[p_loc[i]])
+        new = {}
+        for i in range(S):
+            if keep[i]:
+                new[i] = len(new)
+                tok_out[r, new[i]] = tok[a + i]
+                par_out[r, new[i]] = -1 if i == 0 else new[p_loc[i]]
+        nk = len(new)
+        n_kept[r] = nk
+        anchor = 0
+        if attach == 1:
+            for i in range(S):
+                if keep[i] and (depth[i], c[i]) > (depth[anchor], c[anchor]):
+                    anchor = i
+        F = min(S - nk, len(tparent_bf))
+        for s in range(F):
+            tp = int(tparent_bf[s])
+            src = int(tok[a + anchor]) if tp < 0 else int(tok_out[r, nk + tp])
+            tok_out[r, nk + s] = adj[src, int(trank_bf[s])]
+            par_out[r, nk + s] = new[anchor] if tp < 0 else nk + tp
+    return tok_out, par_out, n_kept
