@@ -379,6 +379,41 @@ def measure_rows(tv, torch, pk, stream):
     for name, d in (("specopd 1024 nodes, trunk 4096", synth.specopd_tree(with_logits=False)),
                     ("blockpilot 8x(8192 prefix + 113 nodes)", synth.blockpilot_sweep(with_mlp=False, V=64))):
         rows[f"tree_verify_attn[{name}]"] = large_tree_row(tv, torch, d, pk, stream)
+    # next rows, per-step planning kernels (kilobytes: launch-bound, reported in µs)
+    rng = np.random.default_rng(7007)
+    B, S = 16, 60
+    par = np.concatenate([synth.random_tree(rng, S, 8) for _ in range(B)]).astype(np.int32)
+    conf = rng.beta(4.0, 1.5, B * S).astype(np.float32)
+    tok = rng.integers(0, V, B * S).astype(np.int32)
+    dp, dc, dt = to_dev(par, torch), to_dev(conf, torch), to_dev(tok, torch)
+    doff = to_dev(np.arange(B + 1, dtype=np.int32) * S, torch)
+    adj = to_dev(synth.successor_table(2), torch)
+    tp, tr = tv.best_first_template(60)
+    so = (torch.empty(B, dtype=torch.int32, device="cuda"), torch.empty((B, 3), dtype=torch.float32, device="cuda"),
+          torch.zeros(1, dtype=torch.int32, device="cuda"))
+    gr = capture(torch, lambda: tv.graft_stage_decide(dp, dc, doff, [0.6, 0.45, 0.2], max_nodes=S, outputs=so), stream)
+    rows["graft_stage_decide[16 trees x 60 nodes]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                       "bound": "launch"}
+    ro = (torch.empty((B, S), dtype=torch.int32, device="cuda"), torch.empty((B, S), dtype=torch.int32, device="cuda"),
+          torch.empty(B, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
+    gr = capture(torch, lambda: tv.graft_replace(dp, dt, dc, S, 0.35, 0, adj, tp, tr, outputs=ro), stream)
+    rows["graft_replace[static, 16 trees x 60 slots]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                          "bound": "launch"}
+    Bt, St = 64, 17
+    tpar = to_dev(np.tile(np.arange(-1, St - 1, dtype=np.int32), Bt), torch)
+    tconf = to_dev(rng.beta(4.0, 1.5, Bt * St).astype(np.float32), torch)
+    ttok = to_dev(rng.integers(0, V, Bt * St).astype(np.int32), torch)
+    to = (torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
+          torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
+          torch.empty(Bt, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
+    gr = capture(torch, lambda: tv.graft_replace(tpar, ttok, tconf, St, 0.3, 1, adj, tp, tr, outputs=to), stream)
+    rows["graft_replace[TAIL, 64 blocks x 16 drafts]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                          "bound": "launch"}
+    dconf = to_dev(synth.dcut_batch(with_attention=False, with_logits=False)["conf"], torch)
+    sc, kp, *_ = tv.dcut_select(dconf, list(synth.DCUT_RHOS))
+    gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream)
+    rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                  "bound": "launch"}
     return rows
 
 

@@ -308,6 +308,67 @@ int dcut_select(const float* conf, int B, int D, const float* rho, int n_rho, fl
                 size_t ws_bytes, tv_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * dcut_choose_rho — expected tokens per budget and the run-time budget choice.
+ * D-cut page, technical summary §2 (runtime adaptive depth selection, budget
+ * selection): the expected gain of a budget, estimated from the drafter's
+ * confidences, over the hardware-profiled cost of a step at that budget;
+ * rho* maximises it.  Reading: the expected gain is the sum of the kept
+ * positions' survival probabilities (a kept root counts 1: the target's own
+ * next token); the cost table is an input (its profiling is not done here).
+ *   score float [B*(D+1)] and keep uint8 [n_rho, B*(D+1)] from dcut_select
+ *   cost  host float [n_rho] > 0: profiled step cost of each budget
+ * Outputs: exp_tok double [n_rho] (NULL allowed); rho_star int32 (device,
+ *   NULL allowed): the budget index maximising exp_tok / cost, lowest on ties.
+ * -------------------------------------------------------------------------- */
+int dcut_choose_rho(const float* score, const uint8_t* keep, int B, int D, int n_rho, const float* cost,
+                    double* exp_tok, int32_t* rho_star, tv_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * graft_stage_decide — Graft's calibrated pruning checkpoints.
+ * Graft page §2 (first gear): the best path's cumulative confidence is
+ * checked at draft layers 0, 1 and 5 only; below the calibrated threshold
+ * the tree stops there and the freed slots go to retrieval (stages 8/52,
+ * 24/36, 40/20; no pruning 60/0).  Readings: a node's draft layer is its
+ * depth - 1 (the root is the current token); its cumulative confidence is
+ * the fp32 product of conf along its path, root excluded, in root-to-node
+ * order; a layer the draft does not reach counts as 0.
+ *   parent int32 [n] request-local (-1 = root), conf float [n] (root unused)
+ *   node_off int32 [B+1]; tau host float [3] thresholds of layers 0, 1, 5
+ * Outputs: stage int32 [B]: first checkpoint whose best value is below its
+ *   threshold (0, 1, 2), else 3; best float [B, 3] or NULL; err (device
+ *   int32, may be NULL) <- 1 for a malformed parent chain (node skipped).
+ * -------------------------------------------------------------------------- */
+int graft_stage_decide(const int32_t* parent, const float* conf, const int32_t* node_off, int B,
+                       int max_nodes, const float* tau, int32_t* stage, float* best, int32_t* err,
+                       tv_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * graft_replace — fixed-slot tree: replace low-confidence draft nodes by
+ * retrieval nodes.
+ * Graft page §4 (batched serving: the per-request slot count stays fixed,
+ * low-confidence nodes of a static tree become retrieval nodes) with
+ * attach = 0; §7 (Graft-TAIL: keep a block draft's confident prefix, replace
+ * its tail by retrieval) with attach = 1 on a chain.
+ * Readings: a draft node is kept when its cumulative confidence (as in
+ * graft_stage_decide) is >= tau and its parent is kept; the S - kept freed
+ * slots take the first slots of a best-first retrieval template, rooted at
+ * the root token (attach 0) or at the deepest kept node (attach 1; ties:
+ * larger cumulative confidence, then lower index).
+ *   Request r's tree is nodes r*S .. r*S+S-1, node 0 of each its root:
+ *   parent int32 [B*S] request-local, tok int32 [B*S], conf float [B*S]
+ *   adj int32 [V, k]; tparent, trank int32 [n_tmpl] best-first template
+ *   (tparent slot-local, -1 = the anchor, < the slot's own index)
+ * Outputs: tok_out, parent_out int32 [B*S] (kept nodes in order, then the
+ *   retrieval slots; -1 padded when the template is shorter), n_kept int32
+ *   [B]; err (device int32, may be NULL) <- 1 for a bad template or table
+ *   entry (that slot is -1) or a malformed parent chain.
+ * -------------------------------------------------------------------------- */
+int graft_replace(const int32_t* parent, const int32_t* tok, const float* conf, int B, int S, float tau,
+                  int attach, const int32_t* adj, int V, int k, const int32_t* tparent, const int32_t* trank,
+                  int n_tmpl, int32_t* tok_out, int32_t* parent_out, int32_t* n_kept, int32_t* err,
+                  tv_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * blockpilot_mlp — BlockPilot's block-size predictor, run once per request.
  * BlockPilot page §3: the full next-token distribution at the last prefill
  * position feeds a two-layer MLP that picks the block size; §7: raw

@@ -15,14 +15,16 @@ import ctypes
 import os
 from typing import Optional, Sequence
 
+import numpy as np
 import torch
 
-from .templates import stage_templates, assemble_hybrid  # noqa: F401  (host-side template data)
+from .templates import stage_template, stage_templates, assemble_hybrid  # noqa: F401  (host-side template data)
 
 __all__ = [
     "TVError", "lib", "tv_tree_prep", "tree_verify_attn", "vocab_argmax_topk", "vocab_argmax_topk_noalloc", "tree_tv_alpha",
     "accept_longest_path", "graft_adj_update", "graft_retrieve", "dcut_select", "blockpilot_mlp",
     "stage_templates", "assemble_hybrid", "LIB_PATH", "load_library", "EXPORTS",
+    "graft_stage_decide", "graft_replace", "dcut_choose_rho", "best_first_template",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtreeverify.so")
@@ -44,6 +46,9 @@ _SIGS = {
     "tree_tv_alpha": (_I, [_P, _P, _I, _I, _I, _I64, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "accept_longest_path": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "graft_adj_update_workspace_size": (_SZ, [_I, _I]),
+    "graft_stage_decide": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
+    "graft_replace": (_I, [_P, _P, _P, _I, _I, ctypes.c_float, _I, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "dcut_choose_rho": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "graft_adj_update": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _P]),
     "graft_retrieve": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dcut_select_workspace_size": (_SZ, [_I, _I, _I]),
@@ -303,6 +308,62 @@ def dcut_select(conf, rhos: Sequence[float], outputs=None):
         _ptr(conf), B, D, rho_host, n_rho, _ptr(score), _ptr(keep), _ptr(keep_len), _ptr(pack_off),
         _ptr(pack_idx), None, 0, _stream()))
     return score, keep, keep_len, pack_off, pack_idx
+
+
+def dcut_choose_rho(score, keep, cost: Sequence[float]):
+    """Expected tokens per budget (float64 [n_rho]) and rho* (int32 [1])."""
+    n_rho, B, N = keep.shape
+    cost_host = (ctypes.c_float * n_rho)(*[float(c) for c in cost])
+    exp_tok = torch.empty(n_rho, dtype=torch.float64, device=score.device)
+    rho_star = torch.empty(1, dtype=torch.int32, device=score.device)
+    _check("dcut_choose_rho", load_library().dcut_choose_rho(
+        _ptr(score), _ptr(keep), B, N - 1, n_rho, cost_host, _ptr(exp_tok), _ptr(rho_star), _stream()))
+    return exp_tok, rho_star
+
+
+# -------------------------------------------------------------- Graft planning
+def best_first_template(S: int = 60, width: int = 8, depth: int = 8, device="cuda"):
+    """(tparent, trank) int32 device tensors: the first S best-first rank paths."""
+    tp, tr = stage_template(S, width, depth)
+    return (torch.from_numpy(np.ascontiguousarray(tp)).to(device),
+            torch.from_numpy(np.ascontiguousarray(tr)).to(device))
+
+
+def graft_stage_decide(parent, conf, node_off, tau: Sequence[float], max_nodes=None, outputs=None):
+    """Returns stage int32 [B], best float32 [B, 3], err int32 [1]."""
+    B = node_off.numel() - 1
+    if max_nodes is None:
+        max_nodes = parent.numel()
+    tau_host = (ctypes.c_float * 3)(*[float(x) for x in tau])
+    if outputs is None:
+        stage = torch.empty(B, dtype=torch.int32, device=parent.device)
+        best = torch.empty((B, 3), dtype=torch.float32, device=parent.device)
+        err = torch.zeros(1, dtype=torch.int32, device=parent.device)
+    else:
+        stage, best, err = outputs
+    _check("graft_stage_decide", load_library().graft_stage_decide(
+        _ptr(parent), _ptr(conf), _ptr(node_off), B, max_nodes, tau_host, _ptr(stage), _ptr(best), _ptr(err),
+        _stream()))
+    return stage, best, err
+
+
+def graft_replace(parent, tok, conf, S: int, tau: float, attach: int, adj, tparent, trank, outputs=None):
+    """Request r's tree = nodes r*S..r*S+S-1.  Returns tok_out, parent_out
+    int32 [B, S], n_kept int32 [B], err int32 [1]."""
+    B = tok.numel() // S
+    V, k = adj.shape
+    dev = tok.device
+    if outputs is None:
+        tok_out = torch.empty((B, S), dtype=torch.int32, device=dev)
+        par_out = torch.empty((B, S), dtype=torch.int32, device=dev)
+        n_kept = torch.empty(B, dtype=torch.int32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    else:
+        tok_out, par_out, n_kept, err = outputs
+    _check("graft_replace", load_library().graft_replace(
+        _ptr(parent), _ptr(tok), _ptr(conf), B, S, float(tau), int(attach), _ptr(adj), V, k, _ptr(tparent),
+        _ptr(trank), tparent.numel(), _ptr(tok_out), _ptr(par_out), _ptr(n_kept), _ptr(err), _stream()))
+    return tok_out, par_out, n_kept, err
 
 
 # --------------------------------------------------------------------- BlockPilot

@@ -217,6 +217,43 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
   }
 }
 
+// Expected tokens per budget (sum of the kept survival probabilities, fp64)
+// and the budget with the best expected tokens per unit of profiled cost.
+// One warp: fp64 arithmetic is scarce on this part, and T <= 8192 terms.
+struct DcutCost { float c[kDcutMaxRho]; };
+
+__global__ void __launch_bounds__(32) dcut_rho_kernel(const float* __restrict__ score,
+                                                      const uint8_t* __restrict__ keep, int T, int n_rho,
+                                                      DcutCost cost, double* __restrict__ exp_tok,
+                                                      int32_t* __restrict__ rho_star) {
+  griddep_wait();
+  griddep_release();
+  const int lane = threadIdx.x;
+  double acc[kDcutMaxRho];
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) acc[a] = 0.0;
+  for (int t = lane; t < T; t += 32) {
+    const double s = static_cast<double>(score[t]);
+#pragma unroll
+    for (int a = 0; a < kDcutMaxRho; ++a)
+      if (a < n_rho && keep[static_cast<int64_t>(a) * T + t]) acc[a] += s;
+  }
+  double best = -1.0;
+  int arg = -1;
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) {
+    double v = acc[a];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (a < n_rho) {
+      if (lane == 0 && exp_tok) exp_tok[a] = v;
+      const double ratio = v / static_cast<double>(cost.c[a]);
+      if (ratio > best) { best = ratio; arg = a; }
+    }
+  }
+  if (lane == 0 && rho_star) *rho_star = arg;
+}
+
 }  // namespace tv
 
 TV_API size_t dcut_select_workspace_size(int B, int D, int n_rho) {
@@ -257,4 +294,21 @@ TV_API int dcut_select(const float* conf, int B, int D, const float* rho, int n_
                                                                                   : tv::dcut_kernel<8>;
   return tv::launch_pdl(kern, dim3(1), dim3(tv::kDcutThreads), bytes, st, conf, B, D, n_rho, ks, score, keep,
                         keep_len, pack_off, pack_idx);
+}
+
+TV_API int dcut_choose_rho(const float* score, const uint8_t* keep, int B, int D, int n_rho, const float* cost,
+                           double* exp_tok, int32_t* rho_star, tv_stream_t stream) {
+  if (B < 0 || D < 0 || n_rho < 0) return TV_EINVAL;
+  if (n_rho > tv::kDcutMaxRho) return TV_EUNSUPPORTED;
+  if (B == 0 || n_rho == 0) return TV_OK;
+  if (!score || !keep || !cost || (!exp_tok && !rho_star)) return TV_EINVAL;
+  const long long T = static_cast<long long>(B) * (D + 1);
+  if (T > tv::kDcutMaxPos) return TV_EUNSUPPORTED;
+  tv::DcutCost c{};
+  for (int a = 0; a < n_rho; ++a) {
+    if (!(cost[a] > 0.f)) return TV_EINVAL;   // host array; positive, not NaN
+    c.c[a] = cost[a];
+  }
+  return tv::launch_pdl(tv::dcut_rho_kernel, dim3(1), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream), score,
+                        keep, static_cast<int>(T), n_rho, c, exp_tok, rho_star);
 }

@@ -38,3 +38,7 @@ def attn_close(o_gpu, o_ref, rel):
     err = np.abs(got - ref).max() if ref.size else 0.0
     scale = np.abs(ref).max() if ref.size else 1.0
     return err <= rel * scale, err, scale
+
+
+def sync():
+    torch.cuda.synchronize()

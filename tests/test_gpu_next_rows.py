@@ -1,0 +1,138 @@
+"""Parity of the next rows' kernels with the oracle: Graft stage decision,
+static-tree replacement and TAIL, D-cut expected tokens and budget choice."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import dev, host, sync
+from oracle import dcut as odc
+from oracle import graft as ogr
+
+pytestmark = pytest.mark.gpu
+
+
+def forest(rng, sizes, depth_bias=0.0):
+    par, off = [], [0]
+    for n in sizes:
+        loc = [-1]
+        for i in range(1, n):
+            lo = max(0, int(i * depth_bias))
+            loc.append(int(rng.integers(lo, i)))
+        par += loc
+        off.append(off[-1] + n)
+    return np.array(par, np.int32), np.array(off, np.int32)
+
+
+# ---------------------------------------------------------------- stage decision
+def check_stage(tv, par, conf, off, tau):
+    st, best, err = tv.graft_stage_decide(dev(par), dev(conf), dev(off), tau, max_nodes=int(np.diff(off).max()))
+    sync()
+    rst, rbest = ogr.stage_decision(par, conf, off, tau)
+    assert np.array_equal(host(best), rbest)          # same fp32 products, same order
+    assert np.array_equal(host(st), rst)
+    assert host(err)[0] == 0
+    return host(st)
+
+
+def test_stage_decide_worked_example(tv, golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "graft_stage_decision.json")))
+    par, conf = np.array(g["parent"], np.int32), np.array(g["conf"], np.float32)
+    for case in g["cases"]:
+        st = check_stage(tv, par, conf, np.array([0, len(par)], np.int32), case["tau"])
+        assert st[0] == case["stage"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_stage_decide_random_forests(tv, seed):
+    rng = np.random.default_rng(seed)
+    sizes = rng.integers(1, 120, 40)
+    sizes[0] = 1                                       # a request with only its root
+    par, off = forest(rng, sizes, depth_bias=0.6)      # deep trees reach layer 5
+    conf = rng.uniform(0.2, 1.0, par.size).astype(np.float32)
+    st = check_stage(tv, par, conf, off, rng.uniform(0.0, 0.6, 3).tolist())
+    assert set(st.tolist()) <= {0, 1, 2, 3}
+
+
+def test_stage_decide_deep_chain(tv):
+    n = 1024
+    par = np.arange(-1, n - 1, dtype=np.int32)
+    conf = np.full(n, 0.999, np.float32)
+    check_stage(tv, par, conf, np.array([0, n], np.int32), [0.5, 0.5, 0.99])
+
+
+# ------------------------------------------------------------ tree replacement
+def check_replace(tv, par, tok, conf, S, tau, attach, adj, tp, tr):
+    B = tok.size // S
+    off = np.arange(B + 1, dtype=np.int32) * S
+    to, po, nk, err = tv.graft_replace(dev(par), dev(tok), dev(conf), S, tau, attach, dev(adj), dev(tp), dev(tr))
+    sync()
+    rto, rpo, rnk = ogr.graft_replace(par, tok, conf, off, S, tau, attach, adj, tp, tr)
+    assert np.array_equal(host(nk), rnk)
+    assert np.array_equal(host(to), rto)
+    assert np.array_equal(host(po), rpo)
+    assert host(err)[0] == 0
+    return rnk
+
+
+@pytest.mark.parametrize("tau", [0.0, 0.3, 0.6, 1.5])
+def test_replace_static_trees(tv, tau):
+    rng = np.random.default_rng(int(tau * 10))
+    B, S, V = 16, 60, synth.QWEN3_VOCAB
+    par, _ = forest(rng, [S] * B, depth_bias=0.3)
+    tok = rng.integers(0, V, B * S).astype(np.int32)
+    conf = rng.uniform(0.3, 1.0, B * S).astype(np.float32)
+    adj = synth.successor_table(2, V, 8)
+    tp, tr = ogr.stage_template(60)
+    nk = check_replace(tv, par, tok, conf, S, tau, 0, adj, tp, tr)
+    if tau == 0.0:
+        assert np.all(nk == S)
+    if tau > 1:
+        assert np.all(nk == 1)
+
+
+@pytest.mark.parametrize("tau", [0.05, 0.2, 0.5])
+def test_replace_tail_of_block_drafts(tv, tau):
+    # DFlash-style 16-token blocks: chains of root + 16 drafts
+    rng = np.random.default_rng(7)
+    B, S, V = 32, 17, 5000
+    par = np.tile(np.arange(-1, S - 1, dtype=np.int32), B)
+    tok = rng.integers(0, V, B * S).astype(np.int32)
+    conf = rng.beta(4, 1.5, B * S).astype(np.float32)
+    adj = rng.integers(0, V, (V, 8)).astype(np.int32)
+    tp, tr = ogr.stage_template(60)
+    check_replace(tv, par, tok, conf, S, tau, 1, adj, tp, tr)
+
+
+def test_replace_short_template_pads(tv):
+    rng = np.random.default_rng(8)
+    B, S, V = 4, 40, 300
+    par, _ = forest(rng, [S] * B)
+    tok = rng.integers(0, V, B * S).astype(np.int32)
+    conf = np.full(B * S, 0.5, np.float32)
+    adj = rng.integers(0, V, (V, 8)).astype(np.int32)
+    tp, tr = ogr.stage_template(10)                    # fewer slots than freed
+    check_replace(tv, par, tok, conf, S, 0.9, 0, adj, tp, tr)
+
+
+# ------------------------------------------------- D-cut expected tokens, rho*
+@pytest.mark.parametrize("which", ["workload", "ones"])
+def test_choose_rho(tv, which):
+    if which == "workload":
+        conf = synth.dcut_batch(with_attention=False, with_logits=False)["conf"]
+        cost = [1.0, 1.35, 1.8, 2.4]
+    else:
+        conf = np.ones((20, 7), np.float32)
+        cost = [1.0, 1.9, 2.95, 3.9]
+    rhos = list(synth.DCUT_RHOS)
+    s, keep, *_ = tv.dcut_select(dev(conf), rhos)
+    E, rs = tv.dcut_choose_rho(s, keep, cost)
+    sync()
+    rs_, rkeep, *_ = odc.select(conf, rhos)
+    rE = odc.expected_tokens(rs_, rkeep)
+    np.testing.assert_allclose(host(E), rE, rtol=1e-12)
+    ratios = np.sort(rE / np.array(cost))
+    assert ratios[-1] - ratios[-2] > 1e-9 * ratios[-1]          # a unique best budget
+    assert host(rs)[0] == odc.choose_rho(rE, cost)
