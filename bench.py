@@ -414,6 +414,27 @@ def measure_rows(tv, torch, pk, stream):
     gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream)
     rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
                                                   "bound": "launch"}
+    # T = 1 verification on the D-cut batch shape: 64 chains of 1 + 15 with
+    # target and draft logits at every node (bf16, 151936); one CTA per
+    # request walks its chain, each visited node costs vocabulary passes
+    Bs, Ns = 64, 16
+    lg_p, lg_q = bf(Bs * Ns, V), bf(Bs * Ns, V)
+    spar = to_dev(np.tile(np.arange(-1, Ns - 1, dtype=np.int32), Bs), torch)
+    soff = to_dev(np.arange(Bs + 1, dtype=np.int32) * Ns, torch)
+    stok = torch.randint(0, V, (Bs * Ns,), generator=g, device="cuda", dtype=torch.int32)
+    su = torch.rand(Bs * Ns, generator=g, device="cuda") * 0.5        # about half the tests accept
+    suf = torch.rand(Bs, generator=g, device="cuda")
+    wss = torch.empty(tv.load_library().accept_rejection_sampling_workspace_size(Bs, V), dtype=torch.uint8,
+                      device="cuda")
+    souts = (torch.empty(Bs, dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"),
+             torch.empty((Bs, Ns), dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"))
+    gr = capture(torch, lambda: tv.accept_rejection_sampling(spar, stok, lg_p, lg_q, soff, su, suf, max_nodes=Ns,
+                                                               max_depth=Ns - 1, ws=wss, outputs=souts), stream)
+    us = time_graph(torch, gr, 20, stream) * 1e3
+    acc_mean = float(souts[0].float().mean())
+    rows["accept_rejection_sampling[T=1, 64 chains of 1+15, V=151936]"] = {
+        "us": round(us, 2), "bound": "latency (sequential walk per request)", "mean_accept_len": round(acc_mean, 2)}
+    del lg_p, lg_q
     return rows
 
 

@@ -236,6 +236,37 @@ int accept_longest_path(const int32_t* parent, const int32_t* tok, const int32_t
                         int32_t* bonus, int32_t* path_acc, tv_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * accept_rejection_sampling — lossless temperature-1 verification.
+ * SpecOPD page §03: under exact rejection sampling the acceptance
+ * probability of a draft token is the draft/target overlap; D-cut page §4
+ * and SpecOPD page §04 report temperature-1 results but give no tree
+ * procedure.  Reading (the standard multi-candidate scheme): from the root,
+ * the children of the current node are tried in index order; child c with
+ * token x is accepted iff u_node[c] < min(1, p'(x) / q(x)), p' = softmax of
+ * the target logits at the current node, q = softmax of the draft logits
+ * there; after each rejection p' becomes max(0, p' - q) renormalised; with
+ * no child accepted the bonus token is the smallest j with
+ * sum_{v <= j} p'(v) > u_final (inverse CDF in token order).
+ *   parent, tok int32 [n] (request-local parents, parents before children)
+ *   p_logits, q_logits [n, ld] dtype: target and draft logits at each node
+ *   u_node float [n] (u of the test that accepts or rejects node i),
+ *   u_final float [B]: uniforms in [0, 1) supplied by the caller
+ *   ws accept_rejection_sampling_workspace_size(B, V) bytes (fp32 residual
+ *   rows), 16-byte aligned
+ * Outputs: accept_len, best_node, bonus int32 [B]; path int32
+ *   [B, max_depth+1] (-1 padded; node indices request-local).
+ * Arithmetic: fp32 exponentials and per-thread sums, fp64 across warps; a
+ * decision whose uniform lies within ~1e-5 of its threshold may differ from
+ * an exact-arithmetic evaluation.
+ * -------------------------------------------------------------------------- */
+size_t accept_rejection_sampling_workspace_size(int B, int V);
+int accept_rejection_sampling(const int32_t* parent, const int32_t* tok, const void* p_logits,
+                              const void* q_logits, int dtype, int V, int64_t ld, const int32_t* node_off,
+                              int B, int max_nodes, int max_depth, const float* u_node, const float* u_final,
+                              int32_t* accept_len, int32_t* best_node, int32_t* path, int32_t* bonus, void* ws,
+                              size_t ws_bytes, tv_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * graft_adj_update — online update of Graft's V x k successor table.
  * Graft page §2 (second/third gear) and §6: after verification, every
  * verified position, accepted or rejected, rewrites the row of its token with
@@ -317,7 +348,8 @@ int dcut_select(const float* conf, int B, int D, const float* rho, int n_rho, fl
  * next token); the cost table is an input (its profiling is not done here).
  *   score float [B*(D+1)] and keep uint8 [n_rho, B*(D+1)] from dcut_select
  *   cost  host float [n_rho] > 0: profiled step cost of each budget
- * Outputs: exp_tok double [n_rho] (NULL allowed); rho_star int32 (device,
+ * Outputs: exp_tok double [n_rho] (NULL allowed): the sum in 2^-50 fixed
+ *   point, within B*(D+1) * 2^-51 of the exact sum; rho_star int32 (device,
  *   NULL allowed): the budget index maximising exp_tok / cost, lowest on ties.
  * -------------------------------------------------------------------------- */
 int dcut_choose_rho(const float* score, const uint8_t* keep, int B, int D, int n_rho, const float* cost,

@@ -20,8 +20,9 @@ the standard multi-candidate scheme (reading, stated here in full):
 Each accepted step leaves the emitted token distributed exactly as the
 target's next-token distribution, which is what makes the scheme lossless;
 the tests pin that property by Monte Carlo.  Arithmetic: float64 from the
-logits (bf16 logits are exact in float64).  A residual that sums to 0
-(p' = q, which cannot reject) keeps p'.
+logits (bf16 logits are exact in float64).  A residual that sums to 0 (only
+possible through rounding: a rejection needs p'(x) < q(x), which leaves
+mass where p' > q) restores p' = softmax(target at the current node).
 """
 from __future__ import annotations
 
@@ -45,14 +46,16 @@ def _row(logits, i):
 def rejection_verify(parent, tok, p_logits, q_logits, node_off, u_node, u_final, max_depth):
     """Returns accept_len int32 [B] (accepted draft nodes), best_node int32 [B]
     (request-local final node), path int32 [B, max_depth+1] (-1 padded),
-    bonus int32 [B], and the trace list of (request, node, p_accept) per
-    child test for test construction."""
+    bonus int32 [B], the trace list of (request, node, p_accept) per child
+    test, and the distribution each bonus token was drawn from (float64 [V]
+    per request) — the last two for test construction."""
     B = len(node_off) - 1
     acc = np.zeros(B, np.int32)
     best = np.zeros(B, np.int32)
     path = np.full((B, max_depth + 1), -1, np.int32)
     bonus = np.zeros(B, np.int32)
     trace = []
+    finals = []
     for r in range(B):
         a, b = int(node_off[r]), int(node_off[r + 1])
         n = b - a
@@ -74,9 +77,9 @@ def rejection_verify(parent, tok, p_logits, q_logits, node_off, u_node, u_final,
                     break
                 res = np.maximum(0.0, pp - q)
                 z = res.sum()
-                if z > 0:
-                    pp = res / z
+                pp = res / z if z > 0 else _softmax64(_row(p_logits, a + cur))
             if nxt < 0:
+                finals.append(pp)
                 cdf = np.cumsum(pp)
                 j = int(np.searchsorted(cdf, u_final[r], side="right"))
                 bonus[r] = min(j, len(pp) - 1)
@@ -87,4 +90,4 @@ def rejection_verify(parent, tok, p_logits, q_logits, node_off, u_node, u_final,
                 path[r, depth] = cur
         acc[r] = depth
         best[r] = cur
-    return acc, best, path, bonus, trace
+    return acc, best, path, bonus, trace, finals

@@ -24,7 +24,7 @@ __all__ = [
     "TVError", "lib", "tv_tree_prep", "tree_verify_attn", "vocab_argmax_topk", "vocab_argmax_topk_noalloc", "tree_tv_alpha",
     "accept_longest_path", "graft_adj_update", "graft_retrieve", "dcut_select", "blockpilot_mlp",
     "stage_templates", "assemble_hybrid", "LIB_PATH", "load_library", "EXPORTS",
-    "graft_stage_decide", "graft_replace", "dcut_choose_rho", "best_first_template",
+    "graft_stage_decide", "graft_replace", "dcut_choose_rho", "best_first_template", "accept_rejection_sampling",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtreeverify.so")
@@ -49,6 +49,9 @@ _SIGS = {
     "graft_stage_decide": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "graft_replace": (_I, [_P, _P, _P, _I, _I, ctypes.c_float, _I, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "dcut_choose_rho": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "accept_rejection_sampling_workspace_size": (_SZ, [_I, _I]),
+    "accept_rejection_sampling": (_I, [_P, _P, _P, _P, _I, _I, _I64, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                      _SZ, _P]),
     "graft_adj_update": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _P]),
     "graft_retrieve": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P]),
     "dcut_select_workspace_size": (_SZ, [_I, _I, _I]),
@@ -319,6 +322,35 @@ def dcut_choose_rho(score, keep, cost: Sequence[float]):
     _check("dcut_choose_rho", load_library().dcut_choose_rho(
         _ptr(score), _ptr(keep), B, N - 1, n_rho, cost_host, _ptr(exp_tok), _ptr(rho_star), _stream()))
     return exp_tok, rho_star
+
+
+def accept_rejection_sampling(parent, tok, p_logits, q_logits, node_off, u_node, u_final, max_nodes=None,
+                              max_depth=None, ws=None, outputs=None):
+    """T = 1 verification.  Returns accept_len, best_node int32 [B], path
+    int32 [B, max_depth+1], bonus int32 [B]."""
+    n, V = p_logits.shape
+    B = node_off.numel() - 1
+    dev = parent.device
+    if max_nodes is None:
+        max_nodes = n
+    if max_depth is None:
+        max_depth = max_nodes - 1
+    dt = _dtype_code(p_logits)
+    need = load_library().accept_rejection_sampling_workspace_size(B, V)
+    if ws is None or ws.numel() < need:
+        ws = _ws(need, dev)
+    if outputs is None:
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        best = torch.empty_like(acc)
+        path = torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev)
+        bonus = torch.empty_like(acc)
+    else:
+        acc, best, path, bonus = outputs
+    _check("accept_rejection_sampling", load_library().accept_rejection_sampling(
+        _ptr(parent), _ptr(tok), _ptr(p_logits), _ptr(q_logits), dt, V, p_logits.stride(0), _ptr(node_off), B,
+        max_nodes, max_depth, _ptr(u_node), _ptr(u_final), _ptr(acc), _ptr(best), _ptr(path), _ptr(bonus),
+        _ptr(ws), ws.numel(), _stream()))
+    return acc, best, path, bonus
 
 
 # -------------------------------------------------------------- Graft planning

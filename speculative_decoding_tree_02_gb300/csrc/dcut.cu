@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
   }
 }
 
-// Expected tokens per budget (sum of the kept survival probabilities, fp64)
-// and the budget with the best expected tokens per unit of profiled cost.
-// One warp: fp64 arithmetic is scarce on this part, and T <= 8192 terms.
+// Expected tokens per budget: the kept survival probabilities summed exactly
+// in fixed point (each score in [0, 1] rounded to a multiple of 2^-50, sums
+// of at most 8192 terms fit 64 bits), so the result is within 8192 * 2^-51
+// of the exact sum whatever the order; then the budget with the best expected
+// tokens per unit of profiled cost.  One warp.
 struct DcutCost { float c[kDcutMaxRho]; };
 
 __global__ void __launch_bounds__(32) dcut_rho_kernel(const float* __restrict__ score,
@@ -229,25 +231,26 @@ __global__ void __launch_bounds__(32) dcut_rho_kernel(const float* __restrict__ 
   griddep_wait();
   griddep_release();
   const int lane = threadIdx.x;
-  double acc[kDcutMaxRho];
+  unsigned long long acc[kDcutMaxRho];
 #pragma unroll
-  for (int a = 0; a < kDcutMaxRho; ++a) acc[a] = 0.0;
+  for (int a = 0; a < kDcutMaxRho; ++a) acc[a] = 0ull;
   for (int t = lane; t < T; t += 32) {
-    const double s = static_cast<double>(score[t]);
+    const unsigned long long fx = __float2ull_rn(fminf(fmaxf(score[t], 0.f), 1.f) * 0x1p50f);
 #pragma unroll
     for (int a = 0; a < kDcutMaxRho; ++a)
-      if (a < n_rho && keep[static_cast<int64_t>(a) * T + t]) acc[a] += s;
+      if (a < n_rho && keep[static_cast<int64_t>(a) * T + t]) acc[a] += fx;
   }
   double best = -1.0;
   int arg = -1;
 #pragma unroll
   for (int a = 0; a < kDcutMaxRho; ++a) {
-    double v = acc[a];
+    unsigned long long v = acc[a];
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (a < n_rho) {
-      if (lane == 0 && exp_tok) exp_tok[a] = v;
-      const double ratio = v / static_cast<double>(cost.c[a]);
+      const double e = static_cast<double>(v) * 0x1p-50;
+      if (lane == 0 && exp_tok) exp_tok[a] = e;
+      const double ratio = e / static_cast<double>(cost.c[a]);
       if (ratio > best) { best = ratio; arg = a; }
     }
   }

@@ -132,7 +132,88 @@ def test_choose_rho(tv, which):
     sync()
     rs_, rkeep, *_ = odc.select(conf, rhos)
     rE = odc.expected_tokens(rs_, rkeep)
-    np.testing.assert_allclose(host(E), rE, rtol=1e-12)
+    np.testing.assert_allclose(host(E), rE, rtol=1e-11)          # 2^-50 fixed point, <= 8192 terms
     ratios = np.sort(rE / np.array(cost))
     assert ratios[-1] - ratios[-2] > 1e-9 * ratios[-1]          # a unique best budget
     assert host(rs)[0] == odc.choose_rho(rE, cost)
+
+
+# ------------------------------------------------ T = 1 rejection sampling
+def sampling_case(seed, sizes, V, dtype="bf16"):
+    """Trees whose children are drawn from the draft softmax of their parent
+    (as the scheme assumes); target logits correlated with the draft's so
+    that paths of several accepts occur."""
+    from oracle import sampling as osm
+    rng = np.random.default_rng(seed)
+    par, off = forest(rng, sizes, depth_bias=0.5)
+    n = par.size
+    base = rng.standard_normal((n, V)).astype(np.float32) * 2.0
+    ql = base + rng.standard_normal((n, V)).astype(np.float32) * 0.5
+    pl = base + rng.standard_normal((n, V)).astype(np.float32) * 0.5
+    if dtype == "bf16":
+        pl, ql = synth.bf16_bits(pl), synth.bf16_bits(ql)
+        pf, qf = osm._row(pl, slice(None)), osm._row(ql, slice(None))
+    else:
+        pf, qf = pl, ql
+    tok = np.zeros(n, np.int32)
+    for r in range(len(sizes)):
+        a = off[r]
+        for i in range(1, sizes[r]):
+            q = osm._softmax64(qf[a + par[a + i]])
+            tok[a + i] = rng.choice(V, p=q)
+    u = rng.random(n).astype(np.float32)
+    uf = rng.random(len(sizes)).astype(np.float32)
+    # keep every uniform that decides a test at least 1e-3 from its threshold
+    for _ in range(20):
+        res = osm.rejection_verify(par, tok, pl, ql, off, u, uf, int(np.diff(off).max()) - 1)
+        close = [(r, c) for r, c, ratio in res[4] if abs(float(u[off[r] + c]) - ratio) < 1e-3]
+        if not close:
+            break
+        for r, c in close:
+            u[off[r] + c] = np.float32(rng.random())
+    return par, off, tok, pl, ql, u, uf, res
+
+
+@pytest.mark.parametrize("seed,dtype", [(0, "bf16"), (1, "bf16"), (2, "f32")])
+def test_rejection_sampling_matches_oracle(tv, seed, dtype):
+    V = 3000 if dtype == "f32" else 5003
+    sizes = [1, 2, 9, 40, 17, 60, 25, 3]
+    par, off, tok, pl, ql, u, uf, (racc, rbest, rpath, rbonus, _, finals) = sampling_case(seed, sizes, V, dtype)
+    max_depth = int(np.diff(off).max()) - 1
+    acc, best, path, bonus = tv.accept_rejection_sampling(dev(par), dev(tok), dev(pl), dev(ql), dev(off), dev(u),
+                                                          dev(uf), max_depth=max_depth)
+    sync()
+    assert np.array_equal(host(acc), racc)
+    assert np.array_equal(host(best), rbest)
+    assert np.array_equal(host(path), rpath)
+    # the bonus token: equal, or u_final within 1e-5 of the CDF step between
+    # the two choices (fp32 exponentials against the float64 oracle)
+    for r, j in enumerate(host(bonus)):
+        if j != rbonus[r]:
+            cdf = np.cumsum(finals[r])
+            lo = cdf[j - 1] if j > 0 else 0.0
+            assert lo - 1e-5 <= uf[r] * cdf[-1] <= cdf[j] + 1e-5, (r, j, rbonus[r])
+    assert np.mean(host(acc)) > 0.3                    # paths with accepts occur
+
+
+def test_rejection_sampling_identical_distributions(tv):
+    # draft = target: every first child is accepted, down to a leaf
+    rng = np.random.default_rng(5)
+    V = 2000
+    par, off = forest(rng, [30, 30, 30], depth_bias=0.4)
+    lg = synth.bf16_bits(rng.standard_normal((par.size, V)).astype(np.float32))
+    tok = rng.integers(0, V, par.size).astype(np.int32)
+    u = (rng.random(par.size) * 0.999).astype(np.float32)
+    uf = rng.random(3).astype(np.float32)
+    acc, best, path, bonus = tv.accept_rejection_sampling(dev(par), dev(tok), dev(lg), dev(lg), dev(off), dev(u),
+                                                          dev(uf), max_depth=29)
+    sync()
+    for r in range(3):
+        loc = par[off[r]:off[r + 1]]
+        cur, d = 0, 0
+        while True:
+            kids = [i for i in range(len(loc)) if loc[i] == cur]
+            if not kids:
+                break
+            cur, d = kids[0], d + 1
+        assert host(acc)[r] == d and host(best)[r] == cur

@@ -19,7 +19,7 @@ def first_token_frequencies(pl, ql, parent, n_sib, trials, seed):
         tok = np.zeros(n, np.int64)
         for i in range(1, n):
             tok[i] = rng.choice(V, p=q[parent[i]])
-        acc, _, path, bonus, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, n]), rng.random(n),
+        acc, _, path, bonus, _, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, n]), rng.random(n),
                                                       rng.random(1), n)
         cnt[tok[path[0, 1]] if acc[0] >= 1 else bonus[0]] += 1
     return cnt / trials
@@ -44,7 +44,7 @@ def test_identical_distributions_accept_every_first_child():
     parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)])
     lg = rng.standard_normal((n, V))
     tok = rng.integers(0, V, n)
-    acc, best, path, _, _ = osm.rejection_verify(parent, tok, lg, lg, np.array([0, n]), rng.random(n) * 0.999,
+    acc, best, path, _, _, _ = osm.rejection_verify(parent, tok, lg, lg, np.array([0, n]), rng.random(n) * 0.999,
                                                  np.array([0.5]), n)
     # expected: follow the lowest-index child at every step down to a leaf
     cur, d = 0, 0
@@ -63,12 +63,12 @@ def test_one_hot_draft_accepts_with_the_target_probability():
     ql = np.array([[-60.0, -60.0, 0.0, -60.0, -60.0], [0.0] * V])   # the draft is sure of token 2
     parent, tok = np.array([-1, 0]), np.array([0, 2])
     for u, want in ((0.29, 1), (0.31, 0)):
-        acc, _, _, _, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, 2]), np.array([0.0, u]),
+        acc, _, _, _, _, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, 2]), np.array([0.0, u]),
                                                np.array([0.5]), 1)
         assert acc[0] == want
     # after that rejection the residual is p without token 2, renormalised:
     # cdf 0.05/0.7, 0.2/0.7, (same), 0.4/0.7, 1 = 0.071, 0.286, 0.286, 0.571, 1
     for uf, want in ((0.25, 1), (0.3, 3), (0.6, 4), (0.05, 0)):
-        _, _, _, bonus, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, 2]), np.array([0.0, 0.9]),
+        _, _, _, bonus, _, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, 2]), np.array([0.0, 0.9]),
                                                  np.array([uf]), 1)
         assert bonus[0] == want
