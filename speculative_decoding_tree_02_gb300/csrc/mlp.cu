@@ -3,7 +3,14 @@
 // block size once per request; §7 raw probabilities as input; §4 hidden 2048;
 // §2 candidates B-3 .. B+3).
 //
-// Layer 1 is a bandwidth-bound GEMV with 8 right-hand sides (the requests):
+// Layer 1, up to 8 requests (tensor cores): D[h, c] = sum_v W1[v, h] X[c, v]
+// with tcgen05 MMAs, M = 128 hidden units per CTA, N = 16: X rows 0..7 are
+// the probabilities rounded to bf16 (x_hi), rows 8..15 the rounding
+// remainders (x_lo = bf16(x - x_hi)), so h = D[., b] + D[., 8 + b] carries x
+// to about 16 mantissa bits.  W1 streams through a TMA ring once (split-K
+// over V across CTAs); its tile is the MN-major A operand, X the K-major B.
+//
+// Fallback layer 1 (more requests): a bandwidth-bound GEMV with 8 right-hand sides (the requests):
 // every W1 element is read once and used for 8 FMAs.  Grid (column block of
 // 256 hidden units, V-slice, request group of 8).  The softmax is fused: the
 // CTA first turns its slice of each request's logits into probabilities
@@ -13,8 +20,9 @@
 // ReLU and the argmax run in one small CTA per request, summing the V-slices
 // in slice order (deterministic).
 #include <algorithm>
+#include <cstring>
 
-#include "tv_common.cuh"
+#include "tc_common.cuh"
 
 namespace tv {
 
@@ -91,6 +99,8 @@ __global__ void __launch_bounds__(256) mlp_l2_kernel(
     const float* __restrict__ b1, const uint16_t* __restrict__ W2, const float* __restrict__ b2,
     int block, float* __restrict__ z, int32_t* __restrict__ choice, int32_t* __restrict__ bsize) {
   __shared__ float s_z[256 / 32][32];
+  griddep_wait();
+  griddep_release();
   const int rq = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float zc[32];
 #pragma unroll
@@ -123,6 +133,179 @@ __global__ void __launch_bounds__(256) mlp_l2_kernel(
   }
 }
 
+// ------------------------------------------------------------ tensor-core layer 1
+constexpr int kQTile = 128;                        // hidden units per CTA (MMA M)
+constexpr int kQK = 64;                            // v per pipeline stage (four K = 16 MMAs)
+constexpr int kQN = 16;                            // x_hi rows 0..7, x_lo rows 8..15 (MMA N)
+constexpr int kQStages = 6;
+constexpr int kQThreads = 192;                     // TMA warp, MMA warp, 4 epilogue warps
+constexpr uint32_t kQAHalf = 64 * kQK * 2;         // 64 hidden x 64 v, bf16: 8 KB
+constexpr uint32_t kQStageBytes = 2 * kQAHalf + kQN * kQK * 2;   // 16 KB + 2 KB
+constexpr uint32_t kQBarOff = kQStages * kQStageBytes;
+constexpr uint32_t kQSmem = kQBarOff + 256 + 1024;  // barriers, TMEM slot, status; 1 KB alignment slack
+constexpr size_t kMlpHdrBytes = 256;               // workspace: status word, then X, then partials
+
+struct MlpMaps { CUtensorMap w1, x; };
+struct MlpTcParams {
+  MlpMaps maps;
+  int H, B, ksteps, kps;
+  float* part;
+  int* err;
+};
+
+// x = softmax(logits) rows as bf16 hi/lo pairs: X[c][v], c < 8 hi, c >= 8 lo;
+// rows of absent requests are zero.  Also clears the status word.
+__global__ void __launch_bounds__(256) mlp_x_kernel(const uint16_t* __restrict__ logits, int64_t ld,
+                                                    const float* __restrict__ row_lse, int B, int V, int Vp,
+                                                    uint16_t* __restrict__ X, int* __restrict__ err) {
+  griddep_wait();
+  griddep_release();
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v == 0 && err) *err = 0;
+  if (v >= V) return;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    uint16_t hi = 0, lo = 0;
+    if (b < B) {
+      const float l = bf16_at(logits + static_cast<int64_t>(b) * ld + v);
+      const float x = ex2(fmaf(l, kLog2e, -row_lse[b] * kLog2e));
+      const __nv_bfloat16 h = __float2bfloat16_rn(x);
+      const __nv_bfloat16 r = __float2bfloat16_rn(x - __bfloat162float(h));
+      hi = *reinterpret_cast<const uint16_t*>(&h);
+      lo = *reinterpret_cast<const uint16_t*>(&r);
+    }
+    X[static_cast<int64_t>(b) * Vp + v] = hi;
+    X[static_cast<int64_t>(8 + b) * Vp + v] = lo;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// CTA (hidden tile, K split).  Every wait is bounded; on expiry the CTA
+// records an error code in the status word, stops, and releases its TMEM.
+__global__ void __launch_bounds__(kQThreads, 2) mlp_tc_kernel(const __grid_constant__ MlpTcParams P) {
+  using namespace tc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ht = blockIdx.x, split = blockIdx.y;
+  const int k0 = split * P.kps, n = max(0, min(P.ksteps, k0 + P.kps) - k0);
+  auto full = [&](int s) { return sb + kQBarOff + 8u * s; };
+  auto empty = [&](int s) { return sb + kQBarOff + 8u * (kQStages + s); };
+  const uint32_t done = sb + kQBarOff + 8u * (2 * kQStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kQBarOff + 8 * (2 * kQStages + 1) + 4);
+  griddep_wait();
+  griddep_release();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const uint32_t tslot = sb + kQBarOff + 8 * (2 * kQStages + 1);
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(tslot) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kQBarOff + 8 * (2 * kQStages + 1));
+  int* err = P.err;
+
+  if (warp == 0) {
+    if (lane == 0) {   // ================= TMA producer
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kQStages;
+        if (i >= kQStages && !mbar_wait(empty(s), ((i / kQStages) - 1) & 1, abort_flag, err, 21)) break;
+        const uint32_t dst = sb + s * kQStageBytes;
+        const int v = (k0 + i) * kQK;
+        mbar_expect_tx(full(s), kQStageBytes);
+        tma_load_2d(dst, &P.maps.w1, ht * kQTile, v, full(s));
+        tma_load_2d(dst + kQAHalf, &P.maps.w1, ht * kQTile + 64, v, full(s));
+        tma_load_2d(dst + 2 * kQAHalf, &P.maps.x, v, 0, full(s));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // ================= MMA issuer
+      // M = 128, N = 16, A MN-major (transpose bit 15), B K-major
+      constexpr uint32_t idesc = idesc_bf16(kQTile, kQN, 0) | (1u << 15);
+      bool ok = true;
+      for (int i = 0; i < n && ok; ++i) {
+        const int s = i % kQStages;
+        ok = mbar_wait(full(s), (i / kQStages) & 1, abort_flag, err, 22);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t abase = sb + s * kQStageBytes, bbase = abase + 2 * kQAHalf;
+#pragma unroll
+        for (int kk = 0; kk < kQK / 16; ++kk)
+          umma_bf16(tmem, sdesc(abase + kk * 2048, kQAHalf, 1024), sdesc(bbase + kk * 32, 16, 1024), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(empty(s));
+      }
+      if (n > 0) umma_commit(done);
+      else mbar_arrive(done);
+    }
+  } else {   // ================= epilogue: D rows of this warp's TMEM lane quarter
+    const bool ok = mbar_wait(done, 0, abort_flag, err, 23);
+    tc_fence_after();
+    uint32_t d[16];
+    tmem_ld16(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), d);
+    tmem_ld_wait();
+    const int h = ht * kQTile + 32 * (warp & 3) + lane;
+    if (ok) {
+      for (int b = 0; b < P.B; ++b) {
+        const float v = n > 0 ? __uint_as_float(d[b]) + __uint_as_float(d[8 + b]) : 0.f;
+        P.part[(static_cast<int64_t>(split) * P.B + b) * P.H + h] = v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+  }
+}
+
+static bool mlp_map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_in, uint32_t box_out) {
+  auto enc = tc::encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// tensor-core path geometry: K splits so that (H / 128) x splits fill two CTAs per SM
+static void mlp_tc_shape(int V, int H, int n_sm, int* ksteps, int* kps, int* splits) {
+  *ksteps = (V + kQK - 1) / kQK;
+  const int tiles = H / kQTile;
+  int s = std::max(1, (2 * n_sm + tiles - 1) / tiles);
+  s = std::min(s, *ksteps);
+  *kps = (*ksteps + s - 1) / s;
+  *splits = (*ksteps + *kps - 1) / *kps;
+}
+
+static bool mlp_tc_ok(int B, int V, int H, int64_t ld, const void* W1) {
+  return B <= 8 && H % kQTile == 0 && (static_cast<int64_t>(H) * 2) % 16 == 0 && aligned(W1, 16) && V >= 1 &&
+         ld >= V;
+}
+
 int mlp_slices(int V, int H, int B) {
   int dev = 0, n_sm = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -135,9 +318,20 @@ int mlp_slices(int V, int H, int B) {
 
 }  // namespace tv
 
+static int sm_count_mlp() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
 TV_API size_t blockpilot_mlp_workspace_size(int B, int V, int H) {
   if (B <= 0 || V <= 0 || H <= 0) return 0;
-  return static_cast<size_t>(tv::mlp_slices(V, H, B)) * B * H * sizeof(float);
+  const size_t simt = static_cast<size_t>(tv::mlp_slices(V, H, B)) * B * H * sizeof(float);
+  int ksteps = 0, kps = 0, splits = 0;
+  tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
+  const size_t Vp = (static_cast<size_t>(V) + 63) / 64 * 64;
+  const size_t tcb = tv::kMlpHdrBytes + 16 * Vp * 2 + static_cast<size_t>(splits) * B * H * sizeof(float);
+  return std::max(simt, tcb);
 }
 
 TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_lse,
@@ -151,9 +345,36 @@ TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_
   if (!tv::aligned(W1, 16)) return TV_EINVAL;
   const size_t need = blockpilot_mlp_workspace_size(B, V, H);
   if (!ws || ws_bytes < need || !tv::aligned(ws, 16)) return TV_EWORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (tv::mlp_tc_ok(B, V, H, ld, W1)) {
+    int ksteps = 0, kps = 0, splits = 0;
+    tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
+    const int Vp = (V + 63) / 64 * 64;
+    char* base = static_cast<char*>(ws);
+    int* err = reinterpret_cast<int*>(base);
+    auto* X = reinterpret_cast<uint16_t*>(base + tv::kMlpHdrBytes);
+    auto* part = reinterpret_cast<float*>(base + tv::kMlpHdrBytes + static_cast<size_t>(16) * Vp * 2);
+    tv::MlpTcParams P;
+    std::memset(&P, 0, sizeof(P));
+    if (!tv::mlp_map2d(&P.maps.w1, W1, static_cast<uint64_t>(H), static_cast<uint64_t>(V),
+                       static_cast<uint64_t>(H) * 2, 64, tv::kQK) ||
+        !tv::mlp_map2d(&P.maps.x, X, static_cast<uint64_t>(V), 16, static_cast<uint64_t>(Vp) * 2, tv::kQK, 16))
+      return TV_ECUDA;
+    P.H = H; P.B = B; P.ksteps = ksteps; P.kps = kps; P.part = part; P.err = err;
+    static const bool attr = cudaFuncSetAttribute(tv::mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(tv::kQSmem)) == cudaSuccess;
+    if (!attr) return TV_ECUDA;
+    int rc = tv::launch_pdl(tv::mlp_x_kernel, dim3((V + 255) / 256), dim3(256), 0, st,
+                            static_cast<const uint16_t*>(last_logits), ld, row_lse, B, V, Vp, X, err);
+    if (rc == TV_OK)
+      rc = tv::launch_pdl(tv::mlp_tc_kernel, dim3(H / tv::kQTile, splits), dim3(tv::kQThreads), tv::kQSmem, st, P);
+    if (rc == TV_OK)
+      rc = tv::launch_pdl(tv::mlp_l2_kernel, dim3(B), dim3(256), 0, st, static_cast<const float*>(part), splits, B,
+                          H, C, b1, static_cast<const uint16_t*>(W2), b2, block, z, choice, bsize);
+    return rc;
+  }
   const int n_slice = tv::mlp_slices(V, H, B);
   const int rows_per_slice = (V + n_slice - 1) / n_slice;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   dim3 g1(H / tv::kMCols, n_slice, (B + tv::kMReq - 1) / tv::kMReq);
   tv::mlp_l1_kernel<<<g1, tv::kMThreads, 0, st>>>(
       static_cast<const uint16_t*>(last_logits), ld, row_lse, static_cast<const uint16_t*>(W1), B,
