@@ -4,14 +4,15 @@
 // sampling is the distribution overlap; E2E-TV multiplies it along a branch.
 // Graft page §3: coverage gain is target probability mass).
 //
-// bf16 rows whose length and stride are multiples of 8 (16 bytes): one read.
-//   A cluster of 8 CTAs per row; CTA c copies its eighth of both rows into
-//   shared memory with bulk copies and keeps it there.  Pass 1 on the slice:
-//   max and sum of exp for p and q; the 8 partials are exchanged through
-//   distributed shared memory, so every CTA knows the row's lse_p, lse_q.
-//   Pass 2 on the same slice: sum of 2^(min(lp - Lp, lq - Lq) log2 e) (one
-//   exponential per element, min taken on the exponents).  CTA 0 adds the 8
-//   overlap partials.  Two CTAs per SM: one copies while the other computes.
+// bf16 rows whose length and stride are multiples of 8 (16 bytes): one read
+// from HBM.  A cluster of 4 CTAs per row, CTA c on a quarter of both rows.
+//   Pass 1 on the slice: running max and sum of exp for p and q; the 4
+//   partials are exchanged through distributed shared memory, so every CTA
+//   knows the row's lse_p, lse_q.  Pass 2 re-reads the slice, still in L2
+//   (a quarter row per CTA keeps the reuse distance far below L2's size):
+//   sum of 2^(min(lp - Lp, lq - Lq) log2 e), one exponential per element,
+//   the min taken on the exponents.  CTA 0 adds the 4 overlap partials.
+//   Clusters are persistent and step through rows.
 // Other rows: two streaming passes over the logits:
 //   pass A  grid (chunks, rows): chunk max and sum of exp for p and q
 //   merge   warp per row: lse_p, lse_q (chunk order, deterministic)
@@ -178,13 +179,8 @@ __global__ void __launch_bounds__(128) alpha_final_kernel(
   }
 }
 
-// Workspace header: status word (nonzero: a copy wait ran out).
+// Workspace: a reserved 256-byte header, then the two-pass partials.
 constexpr size_t kAlphaHdrBytes = 256;
-__global__ void alpha_clear_kernel(int* err) {
-  griddep_wait();
-  griddep_release();
-  *err = 0;
-}
 
 __global__ void alpha_prefix_kernel(const float* __restrict__ alpha, int rows,
                                     const int32_t* __restrict__ branch_off, int nb,
@@ -207,9 +203,8 @@ __global__ void alpha_prefix_kernel(const float* __restrict__ alpha, int rows,
 }
 
 // ------------------------------------------------------------ one-read path
-constexpr int kACluster = 8;
-constexpr int kAClThreads = 256;
-constexpr uint64_t kAlphaTimeoutNs = 2000000000ull;
+constexpr int kACluster = 4;
+constexpr int kAClThreads = 512;
 
 __device__ __forceinline__ uint32_t a_smem(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -225,177 +220,192 @@ __device__ __forceinline__ float cluster_ld(const float* p, uint32_t rank) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
   return v;
 }
+__device__ __forceinline__ float bmax8(uint4 x) {
+  const __nv_bfloat162 h = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&x.x),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&x.y)),
+                                   __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&x.z),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&x.w)));
+  return fmaxf(__low2float(h), __high2float(h));
+}
+// running (max, two partial sums) of exp over 8 bf16 logits
+__device__ __forceinline__ void online8(uint4 x, float& m, float& s0, float& s1) {
+  const float m8 = bmax8(x);
+  if (m8 > m) {   // rescale (the sums are 0 while m is -inf)
+    const float f = ex2((m - m8) * kLog2e);
+    s0 *= f;
+    s1 *= f;
+    m = m8;
+  }
+  if (m != -INFINITY) {
+    const float bm = m * kLog2e;
+    s0 += ex2(fmaf(bf16_lo(x.x), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.x), kLog2e, -bm));
+    s1 += ex2(fmaf(bf16_lo(x.y), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.y), kLog2e, -bm));
+    s0 += ex2(fmaf(bf16_lo(x.z), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.z), kLog2e, -bm));
+    s1 += ex2(fmaf(bf16_lo(x.w), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.w), kLog2e, -bm));
+  }
+}
+// sum over 8 elements of 2^min(lp log2e - Lp, lq log2e - Lq)
+__device__ __forceinline__ void overlap8(uint4 x, uint4 y, float Lp, float Lq, float& a, float& b) {
+  a += ex2(fminf(fmaf(bf16_lo(x.x), kLog2e, -Lp), fmaf(bf16_lo(y.x), kLog2e, -Lq)));
+  b += ex2(fminf(fmaf(bf16_hi(x.x), kLog2e, -Lp), fmaf(bf16_hi(y.x), kLog2e, -Lq)));
+  a += ex2(fminf(fmaf(bf16_lo(x.y), kLog2e, -Lp), fmaf(bf16_lo(y.y), kLog2e, -Lq)));
+  b += ex2(fminf(fmaf(bf16_hi(x.y), kLog2e, -Lp), fmaf(bf16_hi(y.y), kLog2e, -Lq)));
+  a += ex2(fminf(fmaf(bf16_lo(x.z), kLog2e, -Lp), fmaf(bf16_lo(y.z), kLog2e, -Lq)));
+  b += ex2(fminf(fmaf(bf16_hi(x.z), kLog2e, -Lp), fmaf(bf16_hi(y.z), kLog2e, -Lq)));
+  a += ex2(fminf(fmaf(bf16_lo(x.w), kLog2e, -Lp), fmaf(bf16_lo(y.w), kLog2e, -Lq)));
+  b += ex2(fminf(fmaf(bf16_hi(x.w), kLog2e, -Lp), fmaf(bf16_hi(y.w), kLog2e, -Lq)));
+}
 
-// One row per cluster of 8 CTAs; S elements per CTA (multiple of 8).
+// Persistent clusters of 4 CTAs; cluster c takes rows c, c + NC, ...; CTA r
+// of a cluster owns elements [r S, (r + 1) S) of each row (S a multiple of 8).
+// Per row: pass 1 reads the slice from HBM (running max and sum of exp), one
+// cluster barrier makes the 4 slice partials of this row and the 4 overlap
+// partials of the previous row visible, warp 0 forms the row's lse, pass 2
+// re-reads the slice, which a quarter row ago was read into L2, and sums the
+// overlap.  CTA 0 adds the previous row's overlap partials.
 __global__ void __cluster_dims__(kACluster, 1, 1) __launch_bounds__(kAClThreads, 2) alpha_cluster_kernel(
-    const uint16_t* __restrict__ lp, const uint16_t* __restrict__ lq, int V, int64_t ld, int S,
-    const int32_t* __restrict__ mass_tok, float* __restrict__ alpha, float* __restrict__ p_mass,
-    int* __restrict__ err) {
-  extern __shared__ __align__(128) uint8_t sm[];   // [S] p bf16, then [S] q bf16
-  __shared__ __align__(8) uint64_t full;
-  __shared__ float s_red[2][kAClThreads / 32];
-  __shared__ float s_part[4];                        // this CTA's (mp, sp, mq, sq)
-  __shared__ float s_ovl;                            // this CTA's overlap partial
+    const uint16_t* __restrict__ lp, const uint16_t* __restrict__ lq, int rows, int V, int64_t ld, int S,
+    const int32_t* __restrict__ mass_tok, float* __restrict__ alpha, float* __restrict__ p_mass) {
+  __shared__ float s_red[4][kAClThreads / 32];
+  __shared__ float s_ov[kAClThreads / 32];
+  __shared__ float s_part[2][4];   // (mp, sp, mq, sq) of the rows in flight, by parity
+  __shared__ float s_ovl[2];       // overlap partials, by parity
+  __shared__ float s_L[2];         // the current row's lse of p and q (log2 units)
   griddep_wait();
   griddep_release();
   uint32_t rank;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  const int row = blockIdx.x / kACluster;
+  const int NC = gridDim.x / kACluster, cl = blockIdx.x / kACluster;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int base = static_cast<int>(rank) * S;
-  const int n = max(0, min(S, V - base));            // elements of this slice (multiple of 8)
-  const uint16_t* sp_ = reinterpret_cast<const uint16_t*>(sm);
-  const uint16_t* sq_ = sp_ + S;
-  if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a_smem(&full)) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (n > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(n) * 2u;
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a_smem(&full)), "r"(2u * bytes)
-                   : "memory");
-      const uint16_t* gp = lp + static_cast<int64_t>(row) * ld + base;
-      const uint16_t* gq = lq + static_cast<int64_t>(row) * ld + base;
-      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                       a_smem(sp_)),
-                   "l"(gp), "r"(bytes), "r"(a_smem(&full))
-                   : "memory");
-      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                       a_smem(sq_)),
-                   "l"(gq), "r"(bytes), "r"(a_smem(&full))
-                   : "memory");
-    } else {
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a_smem(&full)) : "memory");
+  const int n8 = max(0, min(S, V - base)) / 8;   // 16-byte words of this slice
+  const int K = cl < rows ? (rows - cl + NC - 1) / NC : 0;
+  for (int k = 0; k < K; ++k) {
+    const int b = k & 1, row = cl + k * NC;
+    const uint4* gp = reinterpret_cast<const uint4*>(lp + static_cast<int64_t>(row) * ld + base);
+    const uint4* gq = reinterpret_cast<const uint4*>(lq + static_cast<int64_t>(row) * ld + base);
+    // pass 1
+    float mp = -INFINITY, mq = -INFINITY, sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f;
+    int i = tid;
+    for (; i + kAClThreads < n8; i += 2 * kAClThreads) {
+      const uint4 x0 = __ldg(gp + i), y0 = __ldg(gq + i);
+      const uint4 x1 = __ldg(gp + i + kAClThreads), y1 = __ldg(gq + i + kAClThreads);
+      online8(x0, mp, sp0, sp1);
+      online8(y0, mq, sq0, sq1);
+      online8(x1, mp, sp0, sp1);
+      online8(y1, mq, sq0, sq1);
     }
-  }
-  __syncthreads();
-  // bounded wait for the copies (every CTA still takes part in the cluster
-  // barriers below, so a peer never waits on a CTA that gave up)
-  bool ok = false;
-  {
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-      uint32_t done;
-      asm volatile(
-          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
-          : "=r"(done)
-          : "r"(a_smem(&full))
-          : "memory");
-      if (done) { ok = true; break; }
-      uint64_t t;
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-      if (i == 0) t0 = t;
-      else if (t - t0 > kAlphaTimeoutNs) break;
+    if (i < n8) {
+      online8(__ldg(gp + i), mp, sp0, sp1);
+      online8(__ldg(gq + i), mq, sq0, sq1);
     }
-  }
-  if (!ok && tid == 0 && err) atomicExch(err, 1);
-  const int nv = ok ? n : 0;                         // 8-element vectors below
-  const uint4* vp = reinterpret_cast<const uint4*>(sp_);
-  const uint4* vq = reinterpret_cast<const uint4*>(sq_);
-
-  // pass 1: slice max and sum of exp for p and q
-  __nv_bfloat162 pm2 = __float2bfloat162_rn(-INFINITY), qm2 = pm2;
-  for (int i = tid; i < nv / 8; i += kAClThreads) {
-    const uint4 a = vp[i], b = vq[i];
-    pm2 = __hmax2(pm2, __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a.x),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&a.y)),
-                               __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a.z),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&a.w))));
-    qm2 = __hmax2(qm2, __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&b.x),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&b.y)),
-                               __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&b.z),
-                                       *reinterpret_cast<const __nv_bfloat162*>(&b.w))));
-  }
-  float mp = warp_max(fmaxf(__low2float(pm2), __high2float(pm2)));
-  float mq = warp_max(fmaxf(__low2float(qm2), __high2float(qm2)));
-  if (lane == 0) { s_red[0][warp] = mp; s_red[1][warp] = mq; }
-  __syncthreads();
-  mp = s_red[0][0];
-  mq = s_red[1][0];
+    float spp = sp0 + sp1, sqq = sq0 + sq1;
+    {
+      const float Mp = warp_max(mp), Mq = warp_max(mq);
+      spp = warp_sum(mp == -INFINITY ? 0.f : spp * ex2((mp - Mp) * kLog2e));
+      sqq = warp_sum(mq == -INFINITY ? 0.f : sqq * ex2((mq - Mq) * kLog2e));
+      mp = Mp;
+      mq = Mq;
+    }
+    if (lane == 0) { s_red[0][warp] = mp; s_red[1][warp] = spp; s_red[2][warp] = mq; s_red[3][warp] = sqq; }
+    __syncthreads();
+    if (warp == 0) {   // CTA partial: lane w holds warp w's pair
+      constexpr int W = kAClThreads / 32;
+      const float m0 = lane < W ? s_red[0][lane] : -INFINITY, s0 = lane < W ? s_red[1][lane] : 0.f;
+      const float m1 = lane < W ? s_red[2][lane] : -INFINITY, s1 = lane < W ? s_red[3][lane] : 0.f;
+      const float Mp = warp_max(m0), Mq = warp_max(m1);
+      const float x = warp_sum(m0 == -INFINITY ? 0.f : s0 * ex2((m0 - Mp) * kLog2e));
+      const float y = warp_sum(m1 == -INFINITY ? 0.f : s1 * ex2((m1 - Mq) * kLog2e));
+      if (lane == 0) { s_part[b][0] = Mp; s_part[b][1] = x; s_part[b][2] = Mq; s_part[b][3] = y; }
+    }
+    cluster_sync_all();   // this row's slice partials and the previous row's overlaps are visible
+    if (warp == 0) {
+      if (rank == 0 && k > 0) {
+        const float o = lane < kACluster ? cluster_ld(&s_ovl[b ^ 1], lane) : 0.f;
+        float x = 0.f;
 #pragma unroll
-  for (int w = 1; w < kAClThreads / 32; ++w) { mp = fmaxf(mp, s_red[0][w]); mq = fmaxf(mq, s_red[1][w]); }
-  __syncthreads();
-  float sp = 0.f, sq = 0.f;
-  if (mp != -INFINITY && mq != -INFINITY) {
-    const float bp = mp * kLog2e, bq = mq * kLog2e;
-    for (int i = tid; i < nv / 8; i += kAClThreads) {
-      const uint4 a = vp[i], b = vq[i];
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+        for (int c = 0; c < kACluster; ++c) x += __shfl_sync(0xffffffffu, o, c);
+        if (lane == 0) alpha[row - NC] = x;
+      }
+      float m0 = -INFINITY, s0 = 0.f, m1 = -INFINITY, s1 = 0.f;
+      if (lane < kACluster) {
+        m0 = cluster_ld(&s_part[b][0], lane);
+        s0 = cluster_ld(&s_part[b][1], lane);
+        m1 = cluster_ld(&s_part[b][2], lane);
+        s1 = cluster_ld(&s_part[b][3], lane);
+      }
+      const float Mp = warp_max(m0), Mq = warp_max(m1);
+      const float tp = m0 == -INFINITY ? 0.f : s0 * ex2((m0 - Mp) * kLog2e);
+      const float tq = m1 == -INFINITY ? 0.f : s1 * ex2((m1 - Mq) * kLog2e);
+      float Sp = 0.f, Sq = 0.f;   // slice order
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sp += ex2(fmaf(bf16_lo(wa[k]), kLog2e, -bp)) + ex2(fmaf(bf16_hi(wa[k]), kLog2e, -bp));
-        sq += ex2(fmaf(bf16_lo(wb[k]), kLog2e, -bq)) + ex2(fmaf(bf16_hi(wb[k]), kLog2e, -bq));
+      for (int c = 0; c < kACluster; ++c) {
+        Sp += __shfl_sync(0xffffffffu, tp, c);
+        Sq += __shfl_sync(0xffffffffu, tq, c);
+      }
+      if (lane == 0) {
+        s_L[0] = Mp * kLog2e + log2f(Sp);
+        s_L[1] = Mq * kLog2e + log2f(Sq);
+      }
+    }
+    __syncthreads();
+    const float Lp = s_L[0], Lq = s_L[1];
+    // pass 2
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    i = tid;
+    for (; i + kAClThreads < n8; i += 2 * kAClThreads) {
+      const uint4 x0 = __ldg(gp + i), y0 = __ldg(gq + i);
+      const uint4 x1 = __ldg(gp + i + kAClThreads), y1 = __ldg(gq + i + kAClThreads);
+      overlap8(x0, y0, Lp, Lq, o0, o1);
+      overlap8(x1, y1, Lp, Lq, o2, o3);
+    }
+    if (i < n8) overlap8(__ldg(gp + i), __ldg(gq + i), Lp, Lq, o0, o1);
+    const float ov = warp_sum((o0 + o1) + (o2 + o3));
+    if (lane == 0) s_ov[warp] = ov;
+    __syncthreads();
+    if (warp == 0) {
+      const float x = warp_sum(lane < kAClThreads / 32 ? s_ov[lane] : 0.f);
+      if (lane == 0) {
+        s_ovl[b] = x;
+        if (mass_tok && p_mass) {
+          const int t = mass_tok[row];
+          if (t >= base && t < base + 8 * n8)
+            p_mass[row] = ex2(fmaf(bf16_at(lp + static_cast<int64_t>(row) * ld + t), kLog2e, -Lp));
+          else if (rank == 0 && (t < 0 || t >= V))
+            p_mass[row] = 0.f;
+        }
       }
     }
   }
-  sp = warp_sum(sp);
-  sq = warp_sum(sq);
-  if (lane == 0) { s_red[0][warp] = sp; s_red[1][warp] = sq; }
-  __syncthreads();
-  if (tid == 0) {
-    float a = 0.f, b = 0.f;
+  cluster_sync_all();   // the last row's overlap partials
+  if (rank == 0 && warp == 0 && K > 0) {
+    const float o = lane < kACluster ? cluster_ld(&s_ovl[(K - 1) & 1], lane) : 0.f;
+    float x = 0.f;
 #pragma unroll
-    for (int w = 0; w < kAClThreads / 32; ++w) { a += s_red[0][w]; b += s_red[1][w]; }
-    s_part[0] = mp; s_part[1] = a; s_part[2] = mq; s_part[3] = b;
-  }
-  cluster_sync_all();   // every slice partial is visible to the whole cluster
-
-  // row log-sum-exp (log2 units), the same in every CTA: slice order 0..7
-  float Lp, Lq;
-  {
-    float m[kACluster][2], su[kACluster][2];
-#pragma unroll
-    for (int c = 0; c < kACluster; ++c) {
-      m[c][0] = cluster_ld(&s_part[0], c);
-      su[c][0] = cluster_ld(&s_part[1], c);
-      m[c][1] = cluster_ld(&s_part[2], c);
-      su[c][1] = cluster_ld(&s_part[3], c);
-    }
-    float Mp = -INFINITY, Mq = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kACluster; ++c) { Mp = fmaxf(Mp, m[c][0]); Mq = fmaxf(Mq, m[c][1]); }
-    float Sp = 0.f, Sq = 0.f;
-#pragma unroll
-    for (int c = 0; c < kACluster; ++c) {
-      if (m[c][0] != -INFINITY) Sp += su[c][0] * ex2((m[c][0] - Mp) * kLog2e);
-      if (m[c][1] != -INFINITY) Sq += su[c][1] * ex2((m[c][1] - Mq) * kLog2e);
-    }
-    Lp = Mp * kLog2e + log2f(Sp);
-    Lq = Mq * kLog2e + log2f(Sq);
-  }
-
-  // pass 2: overlap of the slice
-  float ov = 0.f;
-  for (int i = tid; i < nv / 8; i += kAClThreads) {
-    const uint4 a = vp[i], b = vq[i];
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      ov += ex2(fminf(fmaf(bf16_lo(wa[k]), kLog2e, -Lp), fmaf(bf16_lo(wb[k]), kLog2e, -Lq)));
-      ov += ex2(fminf(fmaf(bf16_hi(wa[k]), kLog2e, -Lp), fmaf(bf16_hi(wb[k]), kLog2e, -Lq)));
-    }
-  }
-  ov = warp_sum(ov);
-  if (lane == 0) s_red[0][warp] = ov;
-  __syncthreads();
-  if (tid == 0) {
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < kAClThreads / 32; ++w) a += s_red[0][w];
-    s_ovl = a;
-    if (mass_tok && p_mass) {
-      const int t = mass_tok[row];
-      if (t >= base && t < base + nv) p_mass[row] = ex2(fmaf(bf16_at(sp_ + (t - base)), kLog2e, -Lp));
-      else if (rank == 0 && (t < 0 || t >= V)) p_mass[row] = 0.f;
-    }
-  }
-  cluster_sync_all();
-  if (rank == 0 && tid == 0) {
-    float a = 0.f;
-#pragma unroll
-    for (int c = 0; c < kACluster; ++c) a += cluster_ld(&s_ovl, c);
-    alpha[row] = a;
+    for (int c = 0; c < kACluster; ++c) x += __shfl_sync(0xffffffffu, o, c);
+    if (lane == 0) alpha[cl + (K - 1) * NC] = x;
   }
   cluster_sync_all();   // no CTA leaves while CTA 0 still reads its shared memory
+}
+
+// Clusters that fit at once (a cluster sits in one GPC, so this can be below
+// the SM count times CTAs per SM over the cluster size).
+static int alpha_resident_clusters() {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kACluster);
+  cfg.blockDim = dim3(kAClThreads);
+  cfg.dynamicSmemBytes = 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, alpha_cluster_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    int dev = 0, sms = 8;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    n = std::max(1, 2 * sms / kACluster);
+  }
+  cached = n;
+  return n;
 }
 
 template <typename T>
@@ -406,22 +416,12 @@ int alpha_launch(const T* lp, const T* lq, int rows, int V, int64_t ld, const in
   const bool vec_ok =
       aligned(lp, 16) && aligned(lq, 16) && ((ld * static_cast<int64_t>(sizeof(T))) % 16 == 0);
   if constexpr (sizeof(T) == 2) {
-    // one-read path: 16-byte rows and an eighth of a row that fits shared memory
-    const int S = ((V + kACluster - 1) / kACluster + 7) / 8 * 8;
-    const size_t smem = static_cast<size_t>(S) * 2 * sizeof(uint16_t);
-    if (vec_ok && V % 8 == 0 && ld % 8 == 0 && smem <= 200 * 1024) {
-      static int attr_bytes = 0;
-      if (static_cast<int>(smem) > attr_bytes) {
-        if (cudaFuncSetAttribute(alpha_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-          return TV_ECUDA;
-        attr_bytes = static_cast<int>(smem);
-      }
-      int* err = static_cast<int*>(ws);
-      int rc = launch_pdl(alpha_clear_kernel, dim3(1), dim3(1), 0, st, err);
-      if (rc == TV_OK)
-        rc = launch_pdl(alpha_cluster_kernel, dim3(rows * kACluster), dim3(kAClThreads), smem, st, lp, lq, V, ld, S,
-                        mass_tok, alpha, p_mass, err);
+    // one-read path: 16-byte rows
+    if (vec_ok && V % 8 == 0 && ld % 8 == 0) {
+      const int S = ((V + kACluster - 1) / kACluster + 7) / 8 * 8;
+      const int NC = std::max(1, std::min(rows, alpha_resident_clusters()));
+      int rc = launch_pdl(alpha_cluster_kernel, dim3(NC * kACluster), dim3(kAClThreads), 0, st, lp, lq, rows, V, ld,
+                          S, mass_tok, alpha, p_mass);
       if (rc == TV_OK && alpha_prefix && branch_off)
         rc = launch_pdl(alpha_prefix_kernel, dim3(1), dim3(256), 0, st, alpha, rows, branch_off, nb, alpha_prefix);
       return rc;
