@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row kernel measurements")
+    ap.add_argument("--rows-only", default=None, help="regular expression: measure only the rows of these entry points")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     return ap.parse_args()
 
@@ -318,123 +319,136 @@ def row_entry(us, byts, pk, bound="hbm"):
             "bound": bound}
 
 
-def measure_rows(tv, torch, pk, stream):
+def measure_rows(tv, torch, pk, stream, only=None):
     """Rows of the path on their own workloads, timed with CUDA-graph replays
-    (inputs rotated across enough copies to exceed L2)."""
+    (inputs rotated across enough copies to exceed L2).  `only`: a regular
+    expression; rows whose entry-point names it does not match are skipped."""
+    import re
     rows = {}
+
+    def want(names):
+        return only is None or any(re.search(only, n) for n in names.split("|"))
+
     g = torch.Generator(device="cuda")
     g.manual_seed(5005)
     V = synth.QWEN3_VOCAB
     bf = lambda *s, std=2.0: (torch.randn(s, generator=g, device="cuda") * std).to(torch.bfloat16)
     # a4: alpha on the SpecOPD scoring shape (1024 x 151936, two distributions)
-    lp, lq = bf(1024, V), bf(1024, V)
-    boff = torch.arange(0, 1025, 16, dtype=torch.int32, device="cuda")
-    mtok = torch.randint(0, V, (1024,), generator=g, device="cuda", dtype=torch.int32)
-    ws = torch.empty(tv.load_library().tree_tv_alpha_workspace_size(1024, V), dtype=torch.uint8, device="cuda")
-    o3 = tuple(torch.empty(1024, dtype=torch.float32, device="cuda") for _ in range(3))
-    gr = capture(torch, lambda: tv.tree_tv_alpha(lp, lq, boff, mtok, ws=ws, outputs=o3), stream)
-    rows["tree_tv_alpha[specopd 1024x151936 p,q bf16]"] = row_entry(
-        time_graph(torch, gr, 10, stream) * 1e3, 2 * 1024 * V * 2, pk)
-    del lp, lq, gr
+    if want("tree_tv_alpha"):
+        lp, lq = bf(1024, V), bf(1024, V)
+        boff = torch.arange(0, 1025, 16, dtype=torch.int32, device="cuda")
+        mtok = torch.randint(0, V, (1024,), generator=g, device="cuda", dtype=torch.int32)
+        ws = torch.empty(tv.load_library().tree_tv_alpha_workspace_size(1024, V), dtype=torch.uint8, device="cuda")
+        o3 = tuple(torch.empty(1024, dtype=torch.float32, device="cuda") for _ in range(3))
+        gr = capture(torch, lambda: tv.tree_tv_alpha(lp, lq, boff, mtok, ws=ws, outputs=o3), stream)
+        rows["tree_tv_alpha[specopd 1024x151936 p,q bf16]"] = row_entry(
+            time_graph(torch, gr, 10, stream) * 1e3, 2 * 1024 * V * 2, pk)
+        del lp, lq, gr
     # a3: vocab reductions, Graft single request (61 rows) and D-cut batch (1024 rows)
-    for R in (61, 1024):
-        nc = copies_for(R * V * 2)
-        Ls = [bf(R, V) for _ in range(nc)]
-        wsv = torch.empty(tv.load_library().vocab_argmax_topk_workspace_size(R, V, 8), dtype=torch.uint8,
-                          device="cuda")
-        outs = (torch.empty(R, dtype=torch.int32, device="cuda"), torch.empty((R, 8), dtype=torch.int32, device="cuda"),
-                torch.empty((R, 8), dtype=torch.float32, device="cuda"), torch.empty(R, dtype=torch.float32, device="cuda"),
-                torch.empty(R, dtype=torch.float32, device="cuda"))
-        grs = [capture(torch, lambda L=L: tv.vocab_argmax_topk(L, k=8, ws=wsv, outputs=outs), stream) for L in Ls]
-        rows[f"vocab_argmax_topk[{R}x151936 bf16, k=8, max+lse]"] = row_entry(
-            time_graph(torch, grs, 10 * nc, stream) * 1e3, R * V * 2, pk)
-        del Ls, grs
+    if want("vocab_argmax_topk"):
+        for R in (61, 1024):
+            nc = copies_for(R * V * 2)
+            Ls = [bf(R, V) for _ in range(nc)]
+            wsv = torch.empty(tv.load_library().vocab_argmax_topk_workspace_size(R, V, 8), dtype=torch.uint8,
+                              device="cuda")
+            outs = (torch.empty(R, dtype=torch.int32, device="cuda"), torch.empty((R, 8), dtype=torch.int32, device="cuda"),
+                    torch.empty((R, 8), dtype=torch.float32, device="cuda"), torch.empty(R, dtype=torch.float32, device="cuda"),
+                    torch.empty(R, dtype=torch.float32, device="cuda"))
+            grs = [capture(torch, lambda L=L: tv.vocab_argmax_topk(L, k=8, ws=wsv, outputs=outs), stream) for L in Ls]
+            rows[f"vocab_argmax_topk[{R}x151936 bf16, k=8, max+lse]"] = row_entry(
+                time_graph(torch, grs, 10 * nc, stream) * 1e3, R * V * 2, pk)
+            del Ls, grs
     # a9: BlockPilot MLP (W1 151936 x 2048 bf16 = 622 MB)
-    W1, W2, last = bf(V, 2048, std=0.02), bf(2048, 7, std=0.02), bf(8, V)
-    lse = tv.vocab_argmax_topk(last, k=0)[4]
-    wsm = torch.empty(tv.load_library().blockpilot_mlp_workspace_size(8, V, 2048), dtype=torch.uint8, device="cuda")
-    om = (torch.empty((8, 7), dtype=torch.float32, device="cuda"), torch.empty(8, dtype=torch.int32, device="cuda"),
-          torch.empty(8, dtype=torch.int32, device="cuda"))
-    gr = capture(torch, lambda: tv.blockpilot_mlp(last, lse, W1, W2, ws=wsm, outputs=om), stream)
-    rows["blockpilot_mlp[8x151936->2048->7]"] = row_entry(
-        time_graph(torch, gr, 10, stream) * 1e3, V * 2048 * 2 + 8 * V * 2, pk)
-    del W1, gr
+    if want("blockpilot_mlp"):
+        W1, W2, last = bf(V, 2048, std=0.02), bf(2048, 7, std=0.02), bf(8, V)
+        lse = tv.vocab_argmax_topk(last, k=0)[4]
+        wsm = torch.empty(tv.load_library().blockpilot_mlp_workspace_size(8, V, 2048), dtype=torch.uint8, device="cuda")
+        om = (torch.empty((8, 7), dtype=torch.float32, device="cuda"), torch.empty(8, dtype=torch.int32, device="cuda"),
+              torch.empty(8, dtype=torch.int32, device="cuda"))
+        gr = capture(torch, lambda: tv.blockpilot_mlp(last, lse, W1, W2, ws=wsm, outputs=om), stream)
+        rows["blockpilot_mlp[8x151936->2048->7]"] = row_entry(
+            time_graph(torch, gr, 10, stream) * 1e3, V * 2048 * 2 + 8 * V * 2, pk)
+        del W1, gr
     # a6 bulk form: whole-table update of 151936 rows from a [151936, 8] top-k array
-    nbytes = V * 4 + 2 * V * 8 * 4
-    nc = copies_for(nbytes)
-    sets = [(torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32),
-             torch.randperm(V, device="cuda", generator=g).to(torch.int32),
-             torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32)) for _ in range(nc)]
-    nb = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wsa = torch.empty(max(256, tv.load_library().graft_adj_update_workspace_size(V, V)), dtype=torch.uint8,
-                      device="cuda")
-    grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb, ws=wsa), stream)
-           for a, t, k in sets]
-    rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
-        time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
-    del sets, grs
+    if want("graft_adj_update"):
+        nbytes = V * 4 + 2 * V * 8 * 4
+        nc = copies_for(nbytes)
+        sets = [(torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32),
+                 torch.randperm(V, device="cuda", generator=g).to(torch.int32),
+                 torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32)) for _ in range(nc)]
+        nb = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsa = torch.empty(max(256, tv.load_library().graft_adj_update_workspace_size(V, V)), dtype=torch.uint8,
+                          device="cuda")
+        grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb, ws=wsa), stream)
+               for a, t, k in sets]
+        rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
+            time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
+        del sets, grs
     # a2 on the large-tree shapes, against the bf16 tensor peak: the SpecOPD
     # proposal tree (1024 nodes over one 4096-token trunk, 64 anchors) and the
     # BlockPilot sweep (8 requests x 8192-token prefix x 113 nodes)
-    for name, d in (("specopd 1024 nodes, trunk 4096", synth.specopd_tree(with_logits=False)),
-                    ("blockpilot 8x(8192 prefix + 113 nodes)", synth.blockpilot_sweep(with_mlp=False, V=64))):
-        rows[f"tree_verify_attn[{name}]"] = large_tree_row(tv, torch, d, pk, stream)
+    if want("tree_verify_attn"):
+        for name, d in (("specopd 1024 nodes, trunk 4096", synth.specopd_tree(with_logits=False)),
+                        ("blockpilot 8x(8192 prefix + 113 nodes)", synth.blockpilot_sweep(with_mlp=False, V=64))):
+            rows[f"tree_verify_attn[{name}]"] = large_tree_row(tv, torch, d, pk, stream)
     # next rows, per-step planning kernels (kilobytes: launch-bound, reported in µs)
-    rng = np.random.default_rng(7007)
-    B, S = 16, 60
-    par = np.concatenate([synth.random_tree(rng, S, 8) for _ in range(B)]).astype(np.int32)
-    conf = rng.beta(4.0, 1.5, B * S).astype(np.float32)
-    tok = rng.integers(0, V, B * S).astype(np.int32)
-    dp, dc, dt = to_dev(par, torch), to_dev(conf, torch), to_dev(tok, torch)
-    doff = to_dev(np.arange(B + 1, dtype=np.int32) * S, torch)
-    adj = to_dev(synth.successor_table(2), torch)
-    tp, tr = tv.best_first_template(60)
-    so = (torch.empty(B, dtype=torch.int32, device="cuda"), torch.empty((B, 3), dtype=torch.float32, device="cuda"),
-          torch.zeros(1, dtype=torch.int32, device="cuda"))
-    gr = capture(torch, lambda: tv.graft_stage_decide(dp, dc, doff, [0.6, 0.45, 0.2], max_nodes=S, outputs=so), stream)
-    rows["graft_stage_decide[16 trees x 60 nodes]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
-                                                       "bound": "launch"}
-    ro = (torch.empty((B, S), dtype=torch.int32, device="cuda"), torch.empty((B, S), dtype=torch.int32, device="cuda"),
-          torch.empty(B, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
-    gr = capture(torch, lambda: tv.graft_replace(dp, dt, dc, S, 0.35, 0, adj, tp, tr, outputs=ro), stream)
-    rows["graft_replace[static, 16 trees x 60 slots]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
-                                                          "bound": "launch"}
-    Bt, St = 64, 17
-    tpar = to_dev(np.tile(np.arange(-1, St - 1, dtype=np.int32), Bt), torch)
-    tconf = to_dev(rng.beta(4.0, 1.5, Bt * St).astype(np.float32), torch)
-    ttok = to_dev(rng.integers(0, V, Bt * St).astype(np.int32), torch)
-    to = (torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
-          torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
-          torch.empty(Bt, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
-    gr = capture(torch, lambda: tv.graft_replace(tpar, ttok, tconf, St, 0.3, 1, adj, tp, tr, outputs=to), stream)
-    rows["graft_replace[TAIL, 64 blocks x 16 drafts]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
-                                                          "bound": "launch"}
-    dconf = to_dev(synth.dcut_batch(with_attention=False, with_logits=False)["conf"], torch)
-    sc, kp, *_ = tv.dcut_select(dconf, list(synth.DCUT_RHOS))
-    gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream)
-    rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
-                                                  "bound": "launch"}
+    if want("graft_stage_decide|graft_replace|dcut_choose_rho"):
+        rng = np.random.default_rng(7007)
+        B, S = 16, 60
+        par = np.concatenate([synth.random_tree(rng, S, 8) for _ in range(B)]).astype(np.int32)
+        conf = rng.beta(4.0, 1.5, B * S).astype(np.float32)
+        tok = rng.integers(0, V, B * S).astype(np.int32)
+        dp, dc, dt = to_dev(par, torch), to_dev(conf, torch), to_dev(tok, torch)
+        doff = to_dev(np.arange(B + 1, dtype=np.int32) * S, torch)
+        adj = to_dev(synth.successor_table(2), torch)
+        tp, tr = tv.best_first_template(60)
+        so = (torch.empty(B, dtype=torch.int32, device="cuda"), torch.empty((B, 3), dtype=torch.float32, device="cuda"),
+              torch.zeros(1, dtype=torch.int32, device="cuda"))
+        gr = capture(torch, lambda: tv.graft_stage_decide(dp, dc, doff, [0.6, 0.45, 0.2], max_nodes=S, outputs=so), stream)
+        rows["graft_stage_decide[16 trees x 60 nodes]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                           "bound": "launch"}
+        ro = (torch.empty((B, S), dtype=torch.int32, device="cuda"), torch.empty((B, S), dtype=torch.int32, device="cuda"),
+              torch.empty(B, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
+        gr = capture(torch, lambda: tv.graft_replace(dp, dt, dc, S, 0.35, 0, adj, tp, tr, outputs=ro), stream)
+        rows["graft_replace[static, 16 trees x 60 slots]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                              "bound": "launch"}
+        Bt, St = 64, 17
+        tpar = to_dev(np.tile(np.arange(-1, St - 1, dtype=np.int32), Bt), torch)
+        tconf = to_dev(rng.beta(4.0, 1.5, Bt * St).astype(np.float32), torch)
+        ttok = to_dev(rng.integers(0, V, Bt * St).astype(np.int32), torch)
+        to = (torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
+              torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
+              torch.empty(Bt, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
+        gr = capture(torch, lambda: tv.graft_replace(tpar, ttok, tconf, St, 0.3, 1, adj, tp, tr, outputs=to), stream)
+        rows["graft_replace[TAIL, 64 blocks x 16 drafts]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                              "bound": "launch"}
+        dconf = to_dev(synth.dcut_batch(with_attention=False, with_logits=False)["conf"], torch)
+        sc, kp, *_ = tv.dcut_select(dconf, list(synth.DCUT_RHOS))
+        gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream)
+        rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+                                                      "bound": "launch"}
     # T = 1 verification on the D-cut batch shape: 64 chains of 1 + 15 with
     # target and draft logits at every node (bf16, 151936); one CTA per
     # request walks its chain, each visited node costs vocabulary passes
-    Bs, Ns = 64, 16
-    lg_p, lg_q = bf(Bs * Ns, V), bf(Bs * Ns, V)
-    spar = to_dev(np.tile(np.arange(-1, Ns - 1, dtype=np.int32), Bs), torch)
-    soff = to_dev(np.arange(Bs + 1, dtype=np.int32) * Ns, torch)
-    stok = torch.randint(0, V, (Bs * Ns,), generator=g, device="cuda", dtype=torch.int32)
-    su = torch.rand(Bs * Ns, generator=g, device="cuda") * 0.5        # about half the tests accept
-    suf = torch.rand(Bs, generator=g, device="cuda")
-    wss = torch.empty(tv.load_library().accept_rejection_sampling_workspace_size(Bs, V), dtype=torch.uint8,
-                      device="cuda")
-    souts = (torch.empty(Bs, dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"),
-             torch.empty((Bs, Ns), dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"))
-    gr = capture(torch, lambda: tv.accept_rejection_sampling(spar, stok, lg_p, lg_q, soff, su, suf, max_nodes=Ns,
-                                                               max_depth=Ns - 1, ws=wss, outputs=souts), stream)
-    us = time_graph(torch, gr, 20, stream) * 1e3
-    acc_mean = float(souts[0].float().mean())
-    rows["accept_rejection_sampling[T=1, 64 chains of 1+15, V=151936]"] = {
-        "us": round(us, 2), "bound": "latency (sequential walk per request)", "mean_accept_len": round(acc_mean, 2)}
-    del lg_p, lg_q
+    if want("accept_rejection_sampling"):
+        Bs, Ns = 64, 16
+        lg_p, lg_q = bf(Bs * Ns, V), bf(Bs * Ns, V)
+        spar = to_dev(np.tile(np.arange(-1, Ns - 1, dtype=np.int32), Bs), torch)
+        soff = to_dev(np.arange(Bs + 1, dtype=np.int32) * Ns, torch)
+        stok = torch.randint(0, V, (Bs * Ns,), generator=g, device="cuda", dtype=torch.int32)
+        su = torch.rand(Bs * Ns, generator=g, device="cuda") * 0.5        # about half the tests accept
+        suf = torch.rand(Bs, generator=g, device="cuda")
+        wss = torch.empty(tv.load_library().accept_rejection_sampling_workspace_size(Bs, V), dtype=torch.uint8,
+                          device="cuda")
+        souts = (torch.empty(Bs, dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"),
+                 torch.empty((Bs, Ns), dtype=torch.int32, device="cuda"), torch.empty(Bs, dtype=torch.int32, device="cuda"))
+        gr = capture(torch, lambda: tv.accept_rejection_sampling(spar, stok, lg_p, lg_q, soff, su, suf, max_nodes=Ns,
+                                                                   max_depth=Ns - 1, ws=wss, outputs=souts), stream)
+        us = time_graph(torch, gr, 20, stream) * 1e3
+        acc_mean = float(souts[0].float().mean())
+        rows["accept_rejection_sampling[T=1, 64 chains of 1+15, V=151936]"] = {
+            "us": round(us, 2), "bound": "latency (sequential walk per request)", "mean_accept_len": round(acc_mean, 2)}
+        del lg_p, lg_q
     return rows
 
 
@@ -581,7 +595,7 @@ def gpu_arm(args):
 
     rows = None
     if not args.no_rows and rank == 0:
-        rows = measure_rows(tv, torch, pk, stream)
+        rows = measure_rows(tv, torch, pk, stream, only=args.rows_only)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -613,10 +627,20 @@ def load_traffic(kernel, workload):
         return None
     if not t:
         return None
+    return t["bytes_per_launch"] if source_hash(t["source"]) == t.get("source_sha") else None
+
+
+def source_hash(sources):
+    """First 16 hex digits of the SHA-256 over the named csrc files, in order
+    (a comma-separated list), or None when one is missing."""
     import hashlib
-    src = os.path.join(ROOT, "speculative_decoding_tree_02_gb300", "csrc", t["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
-    return t["bytes_per_launch"] if h == t.get("source_sha") else None
+    h = hashlib.sha256()
+    for name in sources.split(","):
+        p = os.path.join(ROOT, "speculative_decoding_tree_02_gb300", "csrc", name.strip())
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def reference_arm(args):
