@@ -9,7 +9,9 @@ path for the batch:
   -> vocab_argmax_topk (kept rows, k = 8) -> accept_longest_path
   -> graft_adj_update (every verified node's top-8) -> graft_retrieve
      (next step's retrieval candidates from each request's bonus token)
-Metric: verified tree nodes per second (kept positions per step / step time).
+Attention runs on a second stream beside the vocabulary chain (it shares
+only the selection with it).  Metric: verified tree nodes per second (kept
+positions per step / step time).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--rho 0.5] [--impl ours|reference]
 
@@ -227,9 +229,32 @@ def make_step(tv, torch, hd, rho):
                ("vocab_argmax_topk", k_vocab, 2), ("accept_longest_path", k_accept, 1),
                ("graft_adj_update", k_adj, 1), ("graft_retrieve", k_retr, 1)]
 
+    # Dependencies: dcut_select and tv_tree_prep need nothing of each other;
+    # tree_verify_attn needs both; the vocabulary pass needs only the kept
+    # rows, and the acceptance / table update / retrieval chain needs only the
+    # vocabulary results.  So attention runs on a second stream, forked after
+    # the launch of dcut_select and joined at the end of the step, while the
+    # vocabulary chain runs on the caller's stream.
+    side = torch.cuda.Stream(priority=-1)
+    ev_fork, ev_sel, ev_join = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+
     def step():
-        for _, f, _ in kernels:
-            f()
+        cur = torch.cuda.current_stream()
+        ev_fork.record(cur)
+        side.wait_event(ev_fork)
+        with torch.cuda.stream(side):
+            k_prep()
+        k_dcut()
+        ev_sel.record(cur)
+        with torch.cuda.stream(side):
+            side.wait_event(ev_sel)
+            k_attn()
+            ev_join.record(side)
+        k_vocab()
+        k_accept()
+        k_adj()
+        k_retr()
+        cur.wait_event(ev_join)
     return step, kernels, out, K
 
 
