@@ -145,7 +145,12 @@ int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre, const 
  *   top-k    = first k of (value desc, index asc)
  *   row_max  = maximum;  row_lse = max + ln(sum exp(x - max))
  *
- *   logits  [*, ld] dtype, V valid entries per row
+ *   logits  [*, ld] dtype, V valid entries per row, in device memory or in
+ *           page-locked host memory the device addresses directly (e.g.
+ *           cudaHostAlloc; with unified addressing the host pointer is the
+ *           device pointer).  Host-resident rows are read in place over the
+ *           host link, so with row_idx only the selected rows cross it; the
+ *           call then uses a quarter of the SMs.
  *   rows    rows to reduce; row t reads logits row src(t) and writes outputs
  *           at index src(t), where src(t) = row_idx[t] (int32, device) or t
  *   k       0..TV_MAX_TOPK (topk_* may be NULL when k == 0)

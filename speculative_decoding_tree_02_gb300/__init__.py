@@ -110,6 +110,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _ptr_dev_or_pinned(t: torch.Tensor):
+    """Device tensor, or page-locked host tensor that the device reads in place."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("expected a device tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError("libtreeverify takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return TV_F32
@@ -181,13 +190,14 @@ def tree_verify_attn(q, k_pre, v_pre, pre_off, k_tree, v_tree, node_off, anc, ma
 def vocab_argmax_topk(logits, k=8, rows=None, row_idx=None, out_rows=None, want_lse=True,
                       want_max=True, ws=None, outputs=None):
     """Outputs are indexed by source row; with ``row_idx`` give ``out_rows``
-    (the output length, > max(row_idx))."""
+    (the output length, > max(row_idx)).  ``logits`` may be a pinned host
+    tensor: the kernel then reads the rows it needs over the host link."""
     R, V = logits.shape
     dt = _dtype_code(logits)
     if rows is None:
         rows = row_idx.numel() if row_idx is not None else R
     n_out = out_rows if out_rows is not None else R
-    dev = logits.device
+    dev = logits.device if logits.is_cuda else torch.device("cuda", torch.cuda.current_device())
     if outputs is None:
         argmax = torch.full((n_out,), -1, dtype=torch.int32, device=dev)
         tki = torch.empty((n_out, k), dtype=torch.int32, device=dev) if k else None
@@ -200,7 +210,7 @@ def vocab_argmax_topk(logits, k=8, rows=None, row_idx=None, out_rows=None, want_
     if ws is None or ws.numel() < need:
         ws = _ws(need, dev)
     _check("vocab_argmax_topk", load_library().vocab_argmax_topk(
-        _ptr(logits), dt, rows, V, logits.stride(0), _ptr(row_idx), k, _ptr(argmax), _ptr(tki), _ptr(tkv),
+        _ptr_dev_or_pinned(logits), dt, rows, V, logits.stride(0), _ptr(row_idx), k, _ptr(argmax), _ptr(tki), _ptr(tkv),
         _ptr(rmax), _ptr(rlse), _ptr(ws), ws.numel(), _stream()))
     return argmax, tki, tkv, rmax, rlse
 

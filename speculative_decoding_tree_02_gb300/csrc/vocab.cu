@@ -899,6 +899,16 @@ int sm_count_cached() {
   return n;
 }
 
+// True for page-locked host memory the device reads in place.
+static bool host_resident(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
 template <typename T, int KMAX, bool LSE>
 int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* row_idx, int k,
                  int32_t* argmax, int32_t* topk_idx, float* topk_val, float* row_max,
@@ -915,7 +925,10 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
                                                   smem) == cudaSuccess;
     if (!attr) return TV_ECUDA;
     const int items = rows * n_chunks;
-    const int grid = std::min(items, 3 * sm_count_cached());
+    // Rows in page-locked host memory arrive over the host link, far slower
+    // than HBM: a quarter of the SMs keep it busy and leave the rest to
+    // kernels running beside this one.
+    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4) : 3 * sm_count_cached());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
     auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
     int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr);

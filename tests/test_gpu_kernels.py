@@ -149,6 +149,26 @@ def test_vocab_row_gather(tv):
     check_vocab(tv, d["logits"], 8, row_idx=idx)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_vocab_host_resident_rows(tv, dtype):
+    # logits in pinned host memory, read in place: only the gathered rows
+    # are touched; results equal the oracle's (and so the device-resident call's)
+    import torch
+    d = synth.dcut_batch(B=8, V=synth.QWEN3_VOCAB, with_attention=False)
+    x = d["logits"] if dtype == "bf16" else synth.bf16_to_f32(d["logits"])
+    R = x.shape[0]
+    idx = np.array([1, 3, 4, 17, 40, 77, 100, 127], np.int32)
+    xt = torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).pin_memory()
+    am, ti, tvl, rm, rl = tv.vocab_argmax_topk(xt, k=8, row_idx=dev(idx), out_rows=R)
+    sync()
+    ram, rti, rtv, rrm, rrl = ovoc.argmax_topk(x, 8, rows=idx)
+    assert np.array_equal(host(am)[idx], ram)
+    assert np.array_equal(host(ti)[idx], rti)
+    assert np.array_equal(host(tvl)[idx], rtv)
+    assert np.array_equal(host(rm)[idx], rrm)
+    assert np.abs(host(rl)[idx].astype(np.float64) - rrl).max() <= LSE_ATOL
+
+
 def test_vocab_full_size_sample(tv):
     # the D-cut workload at rho = 1: 1024 rows x 151936, checked on a row sample
     d = synth.dcut_batch(with_attention=False)
