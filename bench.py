@@ -518,6 +518,21 @@ def large_tree_row(tv, torch, d, pk, stream):
             "bound": "tensor", "bytes": byts, "gbs": round(byts / us / 1e3, 1)}
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_step):
+    """Units per second over all ranks: every replica verifies its own batch."""
+    return world * units_per_rank / (ms_step / 1e3)
+
+
 def gpu_arm(args):
     import torch
     import speculative_decoding_tree_02_gb300 as tv
@@ -560,13 +575,9 @@ def gpu_arm(args):
             g_step.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, "cuda")
     ms_step = ms_total / args.steps
-    value = world * K / (ms_step / 1e3)
+    value = whole_job_rate(K, world, ms_step)
 
     # per-kernel graphs on the same buffers: average launch duration of each kernel
     per_kernel = {}
@@ -622,8 +633,8 @@ def gpu_arm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host
-    e2e_ms = max(e0.elapsed_time(e1), t_host * 1e3) / n_e2e
-    e2e = {"value": world * K / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), t_host * 1e3) / n_e2e, dist, "cuda")
+    e2e = {"value": whole_job_rate(K, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "inputs": "pinned host memory; small inputs copied per step, logits read in place "
                      "(only the kept rows cross the host link)"}
