@@ -260,9 +260,10 @@ int accept_longest_path(const int32_t* parent, const int32_t* tok, const int32_t
  *   rows), 16-byte aligned
  * Outputs: accept_len, best_node, bonus int32 [B]; path int32
  *   [B, max_depth+1] (-1 padded; node indices request-local).
- * Arithmetic: fp32 exponentials and per-thread sums, fp64 across warps; a
- * decision whose uniform lies within ~1e-5 of its threshold may differ from
- * an exact-arithmetic evaluation.
+ * Arithmetic: fp32 throughout (exponentials, sums, the cross-CTA combines of
+ * the 8-CTA cluster that serves each request); a decision whose uniform lies
+ * within ~1e-5 of its threshold may differ from an exact-arithmetic
+ * evaluation.
  * -------------------------------------------------------------------------- */
 size_t accept_rejection_sampling_workspace_size(int B, int V);
 int accept_rejection_sampling(const int32_t* parent, const int32_t* tok, const void* p_logits,
