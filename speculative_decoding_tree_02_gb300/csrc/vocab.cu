@@ -338,8 +338,9 @@ __global__ void __launch_bounds__(128) vocab_merge_kernel(
 // record.  Nothing is ranked per chunk: the per-row merge ranks all
 // candidates, so a chunk costs one block barrier and no serial section.
 // ---------------------------------------------------------------------------
-// ring of 8192-element chunks: 4 x 16 KB for bf16 (three CTAs per SM), 3 x 32 KB for fp32
-template <typename T> constexpr int stream_stages() { return sizeof(T) == 2 ? 4 : 3; }
+// ring of 8192-element chunks: 3 x 16 KB for bf16 (four CTAs per SM: more chunks in
+// flight per SM beat deeper rings), 3 x 32 KB for fp32
+template <typename T> constexpr int stream_stages() { return 3; }
 template <typename T> constexpr int stream_chunk_bytes() { return kVChunk * static_cast<int>(sizeof(T)); }
 
 __device__ __forceinline__ uint32_t sm_u32(const void* p) {
@@ -493,7 +494,7 @@ __global__ void stream_hdr_clear_kernel(StreamHdr* hdr) {
 constexpr int kStreamThreads = kVThreads + 32;
 
 template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(kStreamThreads, 3) vocab_stream_kernel(
+__global__ void __launch_bounds__(kStreamThreads, 4) vocab_stream_kernel(
     const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows,
     int n_chunks, StreamPart* __restrict__ part, StreamHdr* __restrict__ hdr) {
   constexpr int EPT = kVPerThread;                        // 32 values per thread
@@ -928,7 +929,7 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
     // Rows in page-locked host memory arrive over the host link, far slower
     // than HBM: a quarter of the SMs keep it busy and leave the rest to
     // kernels running beside this one.
-    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4) : 3 * sm_count_cached());
+    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4) : 4 * sm_count_cached());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
     auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
     int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr);
