@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* 
                                                                  int piece_len, int max_pieces, int n_units,
                                                                  int4* __restrict__ plan,
                                                                  int* __restrict__ piece_cnt, int n_cnt,
-                                                                 int* __restrict__ status) {
+                                                                 int n_buckets, int* __restrict__ status) {
   __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets], s_w[33];
   __shared__ int s_base;
   griddep_wait();
@@ -607,13 +607,13 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) { *status = 0; s_base = 0; }
   for (int i = tid; i < n_cnt; i += kPlanThreads) piece_cnt[i] = 0;
-  for (int i = tid; i < kPlanBuckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
+  for (int i = tid; i < n_buckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
   __syncthreads();
   auto shape = [&](int r, int& n, int& bucket) {
     const int Pr = pre_off[r + 1] - pre_off[r];
     n = Pr > 0 ? min((Pr + piece_len - 1) / piece_len, max_pieces) : 1;   // keys past max_prefix: none
     const int last = Pr - (n - 1) * piece_len;
-    bucket = min(kPlanBuckets - 1, (last + 63) / 64);
+    bucket = min(n_buckets - 1, (last + 63) / 64);
   };
   for (int r = tid; r < B; r += kPlanThreads) {
     int n, bk;
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* 
   // bucket starts in decreasing-length order (one warp, suffix sums)
   if (warp == 0) {
     int carry = 0;
-    for (int b0 = kPlanBuckets - 32; b0 >= 0; b0 -= 32) {
+    for (int b0 = n_buckets - 32; b0 >= 0; b0 -= 32) {
       const int b = b0 + 31 - lane;          // lane 0 takes the longest bucket of the group
       int v = s_hist[b], x = v;
 #pragma unroll
@@ -756,8 +756,12 @@ static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long 
   }
   if (!ok) return TV_ECUDA;
   const int tiles = (p.max_nodes + nq - 1) / nq;
+  // 64-key length buckets up to the longest possible last piece, a multiple of 32
+  const int n_buckets = static_cast<int>(std::min<long long>(
+      tc::kPlanBuckets, (std::min<long long>(p.piece_len, p.max_prefix) / 64 + 2 + 31) / 32 * 32));
   int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st, p.pre_off, p.B, p.piece_len,
-                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles, err);
+                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles,
+                      n_buckets, err);
   if (rc != TV_OK) return rc;
   return launch_pdl(tc::attn_tc_kernel<LIVE>, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
 }
