@@ -38,11 +38,20 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  // the stream's priority travels with the launch, so that a kernel captured
+  // into a CUDA graph keeps it (the CTA scheduler serves higher priority first)
+  int prio = 0;
+  if (cudaStreamGetPriority(st, &prio) != cudaSuccess) {
+    cudaGetLastError();
+    prio = 0;
+  }
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = prio;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess ? TV_OK : TV_ECUDA;
 }
 
