@@ -221,30 +221,42 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
 // in fixed point (each score in [0, 1] rounded to a multiple of 2^-50, sums
 // of at most 8192 terms fit 64 bits), so the result is within 8192 * 2^-51
 // of the exact sum whatever the order; then the budget with the best expected
-// tokens per unit of profiled cost.  One warp.
+// tokens per unit of profiled cost.  One CTA of 256 threads: per-thread sums,
+// warp sums, then warp 0 adds the 8 warps' (integer sums: any order is exact).
 struct DcutCost { float c[kDcutMaxRho]; };
+constexpr int kRhoThreads = 256;
 
-__global__ void __launch_bounds__(32) dcut_rho_kernel(const float* __restrict__ score,
-                                                      const uint8_t* __restrict__ keep, int T, int n_rho,
-                                                      DcutCost cost, double* __restrict__ exp_tok,
-                                                      int32_t* __restrict__ rho_star) {
+__global__ void __launch_bounds__(kRhoThreads) dcut_rho_kernel(const float* __restrict__ score,
+                                                               const uint8_t* __restrict__ keep, int T, int n_rho,
+                                                               DcutCost cost, double* __restrict__ exp_tok,
+                                                               int32_t* __restrict__ rho_star) {
+  __shared__ unsigned long long s_acc[kRhoThreads / 32][kDcutMaxRho];
   griddep_wait();
   griddep_release();
-  const int lane = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long acc[kDcutMaxRho];
 #pragma unroll
   for (int a = 0; a < kDcutMaxRho; ++a) acc[a] = 0ull;
-  for (int t = lane; t < T; t += 32) {
+  for (int t = tid; t < T; t += kRhoThreads) {
     const unsigned long long fx = __float2ull_rn(fminf(fmaxf(score[t], 0.f), 1.f) * 0x1p50f);
 #pragma unroll
     for (int a = 0; a < kDcutMaxRho; ++a)
       if (a < n_rho && keep[static_cast<int64_t>(a) * T + t]) acc[a] += fx;
   }
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) {
+    unsigned long long v = acc[a];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_acc[warp][a] = v;
+  }
+  __syncthreads();
+  if (warp != 0) return;
   double best = -1.0;
   int arg = -1;
 #pragma unroll
   for (int a = 0; a < kDcutMaxRho; ++a) {
-    unsigned long long v = acc[a];
+    unsigned long long v = lane < kRhoThreads / 32 ? s_acc[lane][a] : 0ull;
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (a < n_rho) {
@@ -312,6 +324,6 @@ TV_API int dcut_choose_rho(const float* score, const uint8_t* keep, int B, int D
     if (!(cost[a] > 0.f)) return TV_EINVAL;   // host array; positive, not NaN
     c.c[a] = cost[a];
   }
-  return tv::launch_pdl(tv::dcut_rho_kernel, dim3(1), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream), score,
+  return tv::launch_pdl(tv::dcut_rho_kernel, dim3(1), dim3(tv::kRhoThreads), 0, reinterpret_cast<cudaStream_t>(stream), score,
                         keep, static_cast<int>(T), n_rho, c, exp_tok, rho_star);
 }
