@@ -53,7 +53,6 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row kernel measurements")
     ap.add_argument("--rows-only", default=None, help="regular expression: measure only the rows of these entry points")
-    ap.add_argument("--ref-budget-s", type=float, default=120.0)
     return ap.parse_args()
 
 
@@ -76,46 +75,61 @@ def config_dict(rho, n_gpus):
 
 
 # ============================================================ CPU oracle arm
-def _oracle_request(args):
-    """Oracle verification of one request of the batch (run in a worker)."""
-    (r, N, sel, keep_row, parent, tok, logits_rows, q, kt, vt, kp, vp) = args
-    from oracle import accept as oacc, attention as oatt, vocab as ovoc
-    cnt = int(keep_row.sum())
-    off = np.array([0, N], np.int32)
-    oatt.tree_attention(q, kp, vp, np.array([0, kp.shape[0]], np.int32), kt, vt, off, parent,
-                        node_cnt=np.array([cnt]))
-    am, ti, _, _, _ = ovoc.argmax_topk(logits_rows, 8)
+# The oracle runs in spawned worker processes (single-threaded NumPy each).
+# The workload's large arrays sit in shared memory, created once by the
+# parent, so a task carries only indices: one kept position of one request
+# (its attention over all heads and its vocabulary row).
+_SHARED_KEYS = ("q", "k_pre", "v_pre", "k_tree", "v_tree", "logits", "pre_off", "parent")
+_W = {}
+
+
+def _worker_init(specs):
+    from multiprocessing import shared_memory
+    for k, (name, shape, dtype) in specs.items():
+        shm = shared_memory.SharedMemory(name=name)
+        _W[k] = (shm, np.ndarray(shape, dtype=dtype, buffer=shm.buf))
+
+
+def _oracle_node(args):
+    """Oracle of one kept position: tree attention of node (r, j) over its
+    request's prefix and ancestors, all heads; argmax and top-8 of its logits."""
+    r, j, N = args
+    from oracle import attention as oatt, vocab as ovoc
+    a = {k: v[1] for k, v in _W.items()}
+    p0, p1 = int(a["pre_off"][r]), int(a["pre_off"][r + 1])
+    sl = slice(r * N, (r + 1) * N)
+    oatt.tree_attention(a["q"][sl], a["k_pre"][p0:p1], a["v_pre"][p0:p1], np.array([0, p1 - p0], np.int32),
+                        a["k_tree"][sl], a["v_tree"][sl], np.array([0, N], np.int32), a["parent"][sl], nodes=[j])
+    am, ti, _, _, _ = ovoc.argmax_topk(a["logits"][r * N + j:r * N + j + 1], 8)
+    return int(am[0]), ti[0]
+
+
+def oracle_step(d, r, pool, rho, adj, tmpl):
+    """One oracle step on request r's kept positions (selection over the whole
+    batch, then per position attention and vocabulary in the workers, then
+    acceptance, table update and retrieval).  Returns verified nodes."""
+    from oracle import accept as oacc, dcut as odc, graft as ogr
+    N = d["D"] + 1
+    _, keep, keep_len, _, _ = odc.select(d["conf"], [rho])
+    cnt = int(keep_len[0, r])
+    res = pool.map(_oracle_node, [(r, j, N) for j in range(cnt)])
     argmax = np.full(N, -1, np.int32)
-    argmax[:cnt] = am
-    oacc.accept_longest_path(parent, tok, argmax, off, keep_row)
-    return cnt, ti
-
-
-def oracle_step(d, requests, pool, rho, adj, tmpl):
-    """One oracle step on a sample of requests.  Returns verified nodes."""
-    from oracle import dcut as odc, graft as ogr
-    B, N = d["B"], d["D"] + 1
-    s, keep, keep_len, pack_off, pack_idx = odc.select(d["conf"], [rho])
-    jobs = []
-    for r in requests:
-        cnt = int(keep_len[0, r])
-        p0, p1 = int(d["pre_off"][r]), int(d["pre_off"][r + 1])
-        sl = slice(r * N, (r + 1) * N)
-        jobs.append((r, N, None, keep[0, r], d["parent"][sl], d["tok"][sl],
-                     d["logits"][r * N:r * N + cnt], d["q"][sl], d["k_tree"][sl], d["v_tree"][sl],
-                     d["k_pre"][p0:p1], d["v_pre"][p0:p1]))
-    res = pool.map(_oracle_request, jobs) if pool else [_oracle_request(j) for j in jobs]
-    nodes = 0
-    for (r, *_), (cnt, ti) in zip(jobs, res):
-        nodes += cnt
-        ogr.adj_update(adj, d["tok"][r * N:r * N + cnt], ti)
+    ti = np.zeros((cnt, 8), np.int32)
+    for j, (am, t8) in enumerate(res):
+        argmax[j] = am
+        ti[j] = t8
+    sl = slice(r * N, (r + 1) * N)
+    oacc.accept_longest_path(d["parent"][sl], d["tok"][sl], argmax, np.array([0, N], np.int32), keep[0, r])
+    ogr.adj_update(adj, d["tok"][r * N:r * N + cnt], ti)
     tp, tr, off = tmpl
-    ogr.retrieve(adj, d["tok"][[r * N for r in requests]], np.full(len(requests), 2), tp, tr, off, 52)
-    return nodes
+    ogr.retrieve(adj, d["tok"][[r * N]], np.full(1, 2), tp, tr, off, 52)
+    return cnt
 
 
-def run_cpu_oracle(d, rho, steps, warmup, budget_s):
-    """Time the oracle on bounded samples.  Returns (nodes/s, cores, sample text, sec/step)."""
+def run_cpu_oracle(d, rho, steps, warmup):
+    """Time the oracle: W + K steps, step i on request (7 i) mod B.  Returns
+    (nodes/s, cores, sample text, sec/step)."""
+    from multiprocessing import shared_memory
     from oracle import graft as ogr
     tmpl = ogr.stage_templates()
     adj = synth.successor_table(3)
@@ -123,32 +137,38 @@ def run_cpu_oracle(d, rho, steps, warmup, budget_s):
     saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     for k in saved:
         os.environ[k] = "1"
+    shms, specs = [], {}
+    for k in _SHARED_KEYS:
+        arr = np.ascontiguousarray(d[k])
+        shm = shared_memory.SharedMemory(create=True, size=max(1, arr.nbytes))
+        np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
+        shms.append(shm)
+        specs[k] = (shm.name, arr.shape, arr.dtype.str)
     ctx = mp.get_context("spawn")
-    pool = ctx.Pool(cores)
+    pool = ctx.Pool(cores, initializer=_worker_init, initargs=(specs,))
+    B = d["B"]
     try:
-        t0 = time.perf_counter()
-        oracle_step(d, list(range(cores)), pool, rho, adj, tmpl)     # pool start-up + calibration
-        t_one = (time.perf_counter() - t0) / cores
-        per_step = max(budget_s / max(1, steps + warmup), t_one)
-        n_req = int(min(d["B"], max(1, round(per_step / t_one * cores / 2))))
-        reqs = [(7 * i) % d["B"] for i in range(n_req)]
-        for _ in range(warmup):
-            oracle_step(d, reqs, pool, rho, adj, tmpl)
+        oracle_step(d, 0, pool, rho, adj, tmpl)      # pool start-up
+        for i in range(warmup):
+            oracle_step(d, (7 * i) % B, pool, rho, adj, tmpl)
         nodes, t = 0, 0.0
-        for _ in range(steps):
+        for i in range(steps):
             a = time.perf_counter()
-            nodes += oracle_step(d, reqs, pool, rho, adj, tmpl)
+            nodes += oracle_step(d, (7 * (warmup + i)) % B, pool, rho, adj, tmpl)
             t += time.perf_counter() - a
     finally:
         pool.close()
         pool.join()
+        for shm in shms:
+            shm.close()
+            shm.unlink()
         for k, v in saved.items():
             if v is None:
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
-    sample = (f"{n_req} of 64 requests per step (selection over the whole batch), fp64 NumPy oracle, "
-              f"{cores} single-threaded worker processes")
+    sample = (f"one request's kept positions per step (request 7i mod 64; selection over the whole batch), "
+              f"fp64 NumPy oracle, {cores} single-threaded worker processes, one position per task")
     return nodes / t, cores, sample, t / steps
 
 
@@ -670,7 +690,7 @@ def gpu_arm(args):
     if rows:
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample, _ = run_cpu_oracle(d, args.rho, steps=3, warmup=0, budget_s=20.0)
+        v, cores, sample, _ = run_cpu_oracle(d, args.rho, steps=64, warmup=2)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
     if dist:
         dist.barrier()
@@ -713,7 +733,7 @@ def reference_arm(args):
     if rank != 0:
         return
     d = synth.dcut_batch(step=0)
-    v, cores, sample, sec = run_cpu_oracle(d, args.rho, args.steps, args.warmup, args.ref_budget_s)
+    v, cores, sample, sec = run_cpu_oracle(d, args.rho, args.steps, args.warmup)
     line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64; shapes of the D-cut bs=64 workload)",
