@@ -104,31 +104,36 @@ def _oracle_node(args):
     return int(am[0]), ti[0]
 
 
-def oracle_step(d, r, pool, rho, adj, tmpl):
-    """One oracle step on request r's kept positions (selection over the whole
-    batch, then per position attention and vocabulary in the workers, then
-    acceptance, table update and retrieval).  Returns verified nodes."""
+def oracle_step(d, reqs, pool, rho, adj, tmpl):
+    """One oracle step on the kept positions of requests ``reqs`` (selection
+    over the whole batch, then per position attention and vocabulary in the
+    workers, then acceptance, table update and retrieval per request).
+    Returns verified nodes."""
     from oracle import accept as oacc, dcut as odc, graft as ogr
     N = d["D"] + 1
     _, keep, keep_len, _, _ = odc.select(d["conf"], [rho])
-    cnt = int(keep_len[0, r])
-    res = pool.map(_oracle_node, [(r, j, N) for j in range(cnt)])
-    argmax = np.full(N, -1, np.int32)
-    ti = np.zeros((cnt, 8), np.int32)
-    for j, (am, t8) in enumerate(res):
-        argmax[j] = am
-        ti[j] = t8
-    sl = slice(r * N, (r + 1) * N)
-    oacc.accept_longest_path(d["parent"][sl], d["tok"][sl], argmax, np.array([0, N], np.int32), keep[0, r])
-    ogr.adj_update(adj, d["tok"][r * N:r * N + cnt], ti)
+    tasks = [(r, j, N) for r in reqs for j in range(int(keep_len[0, r]))]
+    res = iter(pool.map(_oracle_node, tasks))
+    nodes = 0
     tp, tr, off = tmpl
-    ogr.retrieve(adj, d["tok"][[r * N]], np.full(1, 2), tp, tr, off, 52)
-    return cnt
+    for r in reqs:
+        cnt = int(keep_len[0, r])
+        argmax = np.full(N, -1, np.int32)
+        ti = np.zeros((cnt, 8), np.int32)
+        for j in range(cnt):
+            argmax[j], ti[j] = next(res)
+        sl = slice(r * N, (r + 1) * N)
+        oacc.accept_longest_path(d["parent"][sl], d["tok"][sl], argmax, np.array([0, N], np.int32), keep[0, r])
+        ogr.adj_update(adj, d["tok"][r * N:r * N + cnt], ti)
+        ogr.retrieve(adj, d["tok"][[r * N]], np.full(1, 2), tp, tr, off, 52)
+        nodes += cnt
+    return nodes
 
 
 def run_cpu_oracle(d, rho, steps, warmup):
-    """Time the oracle: W + K steps, step i on request (7 i) mod B.  Returns
-    (nodes/s, cores, sample text, sec/step)."""
+    """Time the oracle: W + K steps, each on the kept positions of cores / 8
+    requests (7 i mod B for the i-th request taken).  Returns (nodes/s,
+    cores, sample text, sec/step)."""
     from multiprocessing import shared_memory
     from oracle import graft as ogr
     tmpl = ogr.stage_templates()
@@ -147,14 +152,16 @@ def run_cpu_oracle(d, rho, steps, warmup):
     ctx = mp.get_context("spawn")
     pool = ctx.Pool(cores, initializer=_worker_init, initargs=(specs,))
     B = d["B"]
+    per = max(1, cores // 8)   # requests per step: about one kept position per worker
+    reqs = lambda i: [(7 * (per * i + q)) % B for q in range(per)]
     try:
-        oracle_step(d, 0, pool, rho, adj, tmpl)      # pool start-up
+        oracle_step(d, [0], pool, rho, adj, tmpl)      # pool start-up
         for i in range(warmup):
-            oracle_step(d, (7 * i) % B, pool, rho, adj, tmpl)
+            oracle_step(d, reqs(i), pool, rho, adj, tmpl)
         nodes, t = 0, 0.0
         for i in range(steps):
             a = time.perf_counter()
-            nodes += oracle_step(d, (7 * (warmup + i)) % B, pool, rho, adj, tmpl)
+            nodes += oracle_step(d, reqs(warmup + i), pool, rho, adj, tmpl)
             t += time.perf_counter() - a
     finally:
         pool.close()
@@ -167,8 +174,8 @@ def run_cpu_oracle(d, rho, steps, warmup):
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
-    sample = (f"one request's kept positions per step (request 7i mod 64; selection over the whole batch), "
-              f"fp64 NumPy oracle, {cores} single-threaded worker processes, one position per task")
+    sample = (f"the kept positions of {per} request(s) per step (requests 7i mod 64; selection over the whole "
+              f"batch), fp64 NumPy oracle, {cores} single-threaded worker processes, one position per task")
     return nodes / t, cores, sample, t / steps
 
 
