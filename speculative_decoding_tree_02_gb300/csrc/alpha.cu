@@ -287,15 +287,18 @@ __global__ void __cluster_dims__(kACluster, 1, 1) __launch_bounds__(kAClThreads,
     // pass 1
     float mp = -INFINITY, mq = -INFINITY, sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f;
     int i = tid;
-    for (; i + kAClThreads < n8; i += 2 * kAClThreads) {
+    for (; i + 2 * kAClThreads < n8; i += 3 * kAClThreads) {   // three vector pairs in flight
       const uint4 x0 = __ldg(gp + i), y0 = __ldg(gq + i);
       const uint4 x1 = __ldg(gp + i + kAClThreads), y1 = __ldg(gq + i + kAClThreads);
+      const uint4 x2 = __ldg(gp + i + 2 * kAClThreads), y2 = __ldg(gq + i + 2 * kAClThreads);
       online8(x0, mp, sp0, sp1);
       online8(y0, mq, sq0, sq1);
       online8(x1, mp, sp0, sp1);
       online8(y1, mq, sq0, sq1);
+      online8(x2, mp, sp0, sp1);
+      online8(y2, mq, sq0, sq1);
     }
-    if (i < n8) {
+    for (; i < n8; i += kAClThreads) {
       online8(__ldg(gp + i), mp, sp0, sp1);
       online8(__ldg(gq + i), mq, sq0, sq1);
     }
@@ -353,13 +356,15 @@ __global__ void __cluster_dims__(kACluster, 1, 1) __launch_bounds__(kAClThreads,
     // pass 2
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     i = tid;
-    for (; i + kAClThreads < n8; i += 2 * kAClThreads) {
+    for (; i + 2 * kAClThreads < n8; i += 3 * kAClThreads) {
       const uint4 x0 = __ldg(gp + i), y0 = __ldg(gq + i);
       const uint4 x1 = __ldg(gp + i + kAClThreads), y1 = __ldg(gq + i + kAClThreads);
+      const uint4 x2 = __ldg(gp + i + 2 * kAClThreads), y2 = __ldg(gq + i + 2 * kAClThreads);
       overlap8(x0, y0, Lp, Lq, o0, o1);
       overlap8(x1, y1, Lp, Lq, o2, o3);
+      overlap8(x2, y2, Lp, Lq, o0, o3);
     }
-    if (i < n8) overlap8(__ldg(gp + i), __ldg(gq + i), Lp, Lq, o0, o1);
+    for (; i < n8; i += kAClThreads) overlap8(__ldg(gp + i), __ldg(gq + i), Lp, Lq, o0, o1);
     const float ov = warp_sum((o0 + o1) + (o2 + o3));
     if (lane == 0) s_ov[warp] = ov;
     __syncthreads();
