@@ -138,6 +138,7 @@ constexpr int kQTile = 128;                        // hidden units per CTA (MMA 
 constexpr int kQK = 64;                            // v per pipeline stage (four K = 16 MMAs)
 constexpr int kQN = 16;                            // x_hi rows 0..7, x_lo rows 8..15 (MMA N)
 constexpr int kQStages = 6;
+constexpr int kQCtas = 2;        // CTAs per SM
 constexpr int kQThreads = 192;                     // TMA warp, MMA warp, 4 epilogue warps
 constexpr uint32_t kQAHalf = 64 * kQK * 2;         // 64 hidden x 64 v, bf16: 8 KB
 constexpr uint32_t kQStageBytes = 2 * kQAHalf + kQN * kQK * 2;   // 16 KB + 2 KB
@@ -190,7 +191,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 // CTA (hidden tile, K split).  Every wait is bounded; on expiry the CTA
 // records an error code in the status word, stops, and releases its TMEM.
-__global__ void __launch_bounds__(kQThreads, 2) mlp_tc_kernel(const __grid_constant__ MlpTcParams P) {
+__global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_constant__ MlpTcParams P) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -291,11 +292,11 @@ static bool mlp_map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// tensor-core path geometry: K splits so that (H / 128) x splits fill two CTAs per SM
+// tensor-core path geometry: K splits so that (H / 128) x splits fill kQCtas CTAs per SM
 static void mlp_tc_shape(int V, int H, int n_sm, int* ksteps, int* kps, int* splits) {
   *ksteps = (V + kQK - 1) / kQK;
   const int tiles = H / kQTile;
-  int s = std::max(1, (2 * n_sm + tiles - 1) / tiles);
+  int s = std::max(1, (kQCtas * n_sm + tiles - 1) / tiles);
   s = std::min(s, *ksteps);
   *kps = (*ksteps + s - 1) / s;
   *splits = (*ksteps + *kps - 1) / *kps;
