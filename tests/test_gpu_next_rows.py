@@ -196,6 +196,25 @@ def test_rejection_sampling_matches_oracle(tv, seed, dtype):
     assert np.mean(host(acc)) > 0.3                    # paths with accepts occur
 
 
+def test_rejection_sampling_full_vocabulary(tv):
+    # the launch configuration the benchmark times: V = 151936 bf16 rows, one
+    # 8-CTA cluster per request, 16-node trees
+    V = synth.QWEN3_VOCAB
+    sizes = [16, 16, 16, 16]
+    par, off, tok, pl, ql, u, uf, (racc, rbest, rpath, rbonus, _, finals) = sampling_case(7, sizes, V, "bf16")
+    acc, best, path, bonus = tv.accept_rejection_sampling(dev(par), dev(tok), dev(pl), dev(ql), dev(off), dev(u),
+                                                          dev(uf), max_depth=15)
+    sync()
+    assert np.array_equal(host(acc), racc)
+    assert np.array_equal(host(best), rbest)
+    assert np.array_equal(host(path), rpath)
+    for r, j in enumerate(host(bonus)):
+        if j != rbonus[r]:
+            cdf = np.cumsum(finals[r])
+            lo = cdf[j - 1] if j > 0 else 0.0
+            assert lo - 1e-5 <= uf[r] * cdf[-1] <= cdf[j] + 1e-5, (r, j, rbonus[r])
+
+
 def test_rejection_sampling_identical_distributions(tv):
     # draft = target: every first child is accepted, down to a leaf
     rng = np.random.default_rng(5)
