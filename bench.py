@@ -389,6 +389,7 @@ def measure_rows(tv, torch, pk, stream, only=None):
     bf = lambda *s, std=2.0: (torch.randn(s, generator=g, device="cuda") * std).to(torch.bfloat16)
     # a4: alpha on the SpecOPD scoring shape (1024 x 151936, two distributions)
     if want("tree_tv_alpha"):
+        g.manual_seed(5005 + 0)   # each row draws its own inputs
         lp, lq = bf(1024, V), bf(1024, V)
         boff = torch.arange(0, 1025, 16, dtype=torch.int32, device="cuda")
         mtok = torch.randint(0, V, (1024,), generator=g, device="cuda", dtype=torch.int32)
@@ -400,6 +401,7 @@ def measure_rows(tv, torch, pk, stream, only=None):
         del lp, lq, gr
     # a3: vocab reductions, Graft single request (61 rows) and D-cut batch (1024 rows)
     if want("vocab_argmax_topk"):
+        g.manual_seed(5005 + 1)   # each row draws its own inputs
         for R in (61, 1024):
             nc = copies_for(R * V * 2)
             Ls = [bf(R, V) for _ in range(nc)]
@@ -414,6 +416,7 @@ def measure_rows(tv, torch, pk, stream, only=None):
             del Ls, grs
     # a9: BlockPilot MLP (W1 151936 x 2048 bf16 = 622 MB)
     if want("blockpilot_mlp"):
+        g.manual_seed(5005 + 2)   # each row draws its own inputs
         W1, W2, last = bf(V, 2048, std=0.02), bf(2048, 7, std=0.02), bf(8, V)
         lse = tv.vocab_argmax_topk(last, k=0)[4]
         wsm = torch.empty(tv.load_library().blockpilot_mlp_workspace_size(8, V, 2048), dtype=torch.uint8, device="cuda")
@@ -425,6 +428,7 @@ def measure_rows(tv, torch, pk, stream, only=None):
         del W1, gr
     # a6 bulk form: whole-table update of 151936 rows from a [151936, 8] top-k array
     if want("graft_adj_update"):
+        g.manual_seed(5005 + 3)   # each row draws its own inputs
         nbytes = V * 4 + 2 * V * 8 * 4
         nc = copies_for(nbytes)
         sets = [(torch.randint(0, V, (V, 8), generator=g, device="cuda", dtype=torch.int32),
@@ -442,11 +446,13 @@ def measure_rows(tv, torch, pk, stream, only=None):
     # proposal tree (1024 nodes over one 4096-token trunk, 64 anchors) and the
     # BlockPilot sweep (8 requests x 8192-token prefix x 113 nodes)
     if want("tree_verify_attn"):
+        g.manual_seed(5005 + 4)   # each row draws its own inputs
         for name, d in (("specopd 1024 nodes, trunk 4096", synth.specopd_tree(with_logits=False)),
                         ("blockpilot 8x(8192 prefix + 113 nodes)", synth.blockpilot_sweep(with_mlp=False, V=64))):
             rows[f"tree_verify_attn[{name}]"] = large_tree_row(tv, torch, d, pk, stream)
     # next rows, per-step planning kernels (kilobytes: launch-bound, reported in µs)
     if want("graft_stage_decide|graft_replace|dcut_choose_rho"):
+        g.manual_seed(5005 + 5)   # each row draws its own inputs
         rng = np.random.default_rng(7007)
         B, S = 16, 60
         par = np.concatenate([synth.random_tree(rng, S, 8) for _ in range(B)]).astype(np.int32)
@@ -485,6 +491,7 @@ def measure_rows(tv, torch, pk, stream, only=None):
     # target and draft logits at every node (bf16, 151936); one CTA per
     # request walks its chain, each visited node costs vocabulary passes
     if want("accept_rejection_sampling"):
+        g.manual_seed(5005 + 6)   # each row draws its own inputs
         Bs, Ns = 64, 16
         lg_p, lg_q = bf(Bs * Ns, V), bf(Bs * Ns, V)
         spar = to_dev(np.tile(np.arange(-1, Ns - 1, dtype=np.int32), Bs), torch)
