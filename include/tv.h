@@ -58,7 +58,7 @@ enum tv_status {
 
 enum tv_dtype { TV_F32 = 0, TV_BF16 = 1 };
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define TV_MAX_NODES 1024   /* nodes per request (tree_prep, attention, acceptance) */
 #define TV_MAX_TOPK 16      /* k of vocab_argmax_topk / graft tables               */
 
