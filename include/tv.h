@@ -416,7 +416,7 @@ int graft_replace(const int32_t* parent, const int32_t* tok, const float* conf, 
  *   bsize = block - (C-1)/2 + choice
  *
  *   last_logits [B, ld] bf16; row_lse float [B]; W1 bf16 [V, H]; W2 bf16 [H, C];
- *   b1 float [H] or NULL; b2 float [C] or NULL.  H % 8 == 0, C <= 32, B <= 16.
+ *   b1 float [H] or NULL; b2 float [C] or NULL.  H % 256 == 0, C <= 32, B <= 16.
  *   Up to 8 requests with H % 128 == 0 run layer 1 on the tensor cores: x is
  *   split into bf16 x_hi + x_lo (about 16 mantissa bits) against bf16 W1,
  *   fp32 accumulation; otherwise a CUDA-core GEMV in fp32.

@@ -149,20 +149,32 @@ constexpr size_t kMlpHdrBytes = 256;               // workspace: status word, th
 struct MlpMaps { CUtensorMap w1, x; };
 struct MlpTcParams {
   MlpMaps maps;
-  int H, B, ksteps, kps;
-  float* part;
+  int H, B, C, block, ksteps, kps;
+  float* part;          // [splits][B][H] layer-1 partial sums
   int* err;
+  int* cnt;             // [tiles + 1] arrival counters, zero between calls
+  float* zpart;         // [tiles][B][C] layer-2 partial sums
+  const float* b1;
+  const uint16_t* W2;
+  const float* b2;
+  float* z;
+  int32_t* choice;
+  int32_t* bsize;
 };
 
 // x = softmax(logits) rows as bf16 hi/lo pairs: X[c][v], c < 8 hi, c >= 8 lo;
-// rows of absent requests are zero.  Also clears the status word.
+// rows of absent requests are zero.  Also clears the status word and the
+// layer-1 kernel's arrival counters.
 __global__ void __launch_bounds__(256) mlp_x_kernel(const uint16_t* __restrict__ logits, int64_t ld,
                                                     const float* __restrict__ row_lse, int B, int V, int Vp,
-                                                    uint16_t* __restrict__ X, int* __restrict__ err) {
+                                                    uint16_t* __restrict__ X, int* __restrict__ err,
+                                                    int* __restrict__ cnt, int n_cnt) {
   griddep_wait();
   griddep_release();
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v == 0 && err) *err = 0;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
   if (v >= V) return;
 #pragma unroll
   for (int b = 0; b < 8; ++b) {
@@ -191,6 +203,11 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 // CTA (hidden tile, K split).  Every wait is bounded; on expiry the CTA
 // records an error code in the status word, stops, and releases its TMEM.
+// Tail: the last split of a hidden tile to finish (arrival counter) sums the
+// tile's partials in split order, adds b1, applies the ReLU and forms the
+// tile's share of layer 2; the last tile to finish sums those shares in tile
+// order, adds b2 and takes the argmax.  Both orders are fixed, so the result
+// does not depend on which CTA happens to arrive last.
 __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_constant__ MlpTcParams P) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
@@ -264,11 +281,14 @@ __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_
     tmem_ld_wait();
     const int h = ht * kQTile + 32 * (warp & 3) + lane;
     if (ok) {
-      for (int b = 0; b < P.B; ++b) {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b >= P.B) break;
         const float v = n > 0 ? __uint_as_float(d[b]) + __uint_as_float(d[8 + b]) : 0.f;
         P.part[(static_cast<int64_t>(split) * P.B + b) * P.H + h] = v;
       }
     }
+    __threadfence();
   }
   tc_fence_before();
   __syncthreads();
@@ -276,6 +296,100 @@ __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+  }
+
+  // ---------------- tail: split-K reduction, ReLU, layer 2, argmax
+  const int tiles = gridDim.x, splits = gridDim.y;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(sm + kQBarOff + 8 * (2 * kQStages + 2));
+  if (threadIdx.x == 0) *s_flag = atomicAdd(&P.cnt[ht], 1) == splits - 1;
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  if (threadIdx.x == 0) P.cnt[ht] = 0;
+  // The ring is free (every MMA has completed): stage 0 holds the tile's W2
+  // rows (128 x C bf16, contiguous in W2) and, later, the layer-2 shares.
+  uint16_t* s_w2 = reinterpret_cast<uint16_t*>(sm);
+  float* s_z = reinterpret_cast<float*>(sm + 8192);              // [B][C]
+  float* s_zp = reinterpret_cast<float*>(sm + 8192 + 1024);      // [tiles][B][C]
+  {
+    const uint16_t* src = P.W2 + static_cast<int64_t>(ht) * kQTile * P.C;
+#pragma unroll 8
+    for (int i = threadIdx.x; i < kQTile * P.C; i += blockDim.x) s_w2[i] = src[i];
+  }
+  // lane q owns hidden units 4q .. 4q+3 of the tile; warp w < 4 requests w and w + 4
+  const int q = lane, h0 = ht * kQTile + 4 * q;
+  const int rb0 = warp, rb1 = warp + 4;
+  const bool has0 = warp < 4 && rb0 < P.B, has1 = warp < 4 && rb1 < P.B;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (warp < 4 && P.b1) a0 = *reinterpret_cast<const float4*>(P.b1 + h0);
+  float4 a1 = a0;
+  {
+    const int64_t sstride = static_cast<int64_t>(P.B) * P.H;
+    const float* p0 = P.part + static_cast<int64_t>(rb0) * P.H + h0;
+    const float* p1 = P.part + static_cast<int64_t>(rb1) * P.H + h0;
+#pragma unroll 8
+    for (int s = 0; s < splits; ++s) {   // split order
+      if (has0) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(p0 + s * sstride));
+        a0.x += t.x; a0.y += t.y; a0.z += t.z; a0.w += t.w;
+      }
+      if (has1) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(p1 + s * sstride));
+        a1.x += t.x; a1.y += t.y; a1.z += t.z; a1.w += t.w;
+      }
+    }
+  }
+  __syncthreads();   // W2 rows staged
+  if (warp < 4) {
+    const float r0[4] = {fmaxf(a0.x, 0.f), fmaxf(a0.y, 0.f), fmaxf(a0.z, 0.f), fmaxf(a0.w, 0.f)};
+    const float r1[4] = {fmaxf(a1.x, 0.f), fmaxf(a1.y, 0.f), fmaxf(a1.z, 0.f), fmaxf(a1.w, 0.f)};
+    for (int c = 0; c < P.C; ++c) {
+      float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float w = __uint_as_float(static_cast<uint32_t>(s_w2[(4 * q + i) * P.C + c]) << 16);
+        z0 = fmaf(r0[i], w, z0);
+        z1 = fmaf(r1[i], w, z1);
+      }
+      z0 = warp_sum(z0);
+      z1 = warp_sum(z1);
+      if (q == 0 && has0) P.zpart[(static_cast<int64_t>(ht) * P.B + rb0) * P.C + c] = z0;
+      if (q == 0 && has1) P.zpart[(static_cast<int64_t>(ht) * P.B + rb1) * P.C + c] = z1;
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = atomicAdd(&P.cnt[tiles], 1) == tiles - 1;
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  if (threadIdx.x == 0) P.cnt[tiles] = 0;
+  const int n_zp = tiles * P.B * P.C;
+  const bool staged = static_cast<uint32_t>(n_zp) * 4u <= kQBarOff - 8192u - 1024u;
+  if (staged) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n_zp; i += blockDim.x) s_zp[i] = __ldcg(P.zpart + i);
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < P.B * P.C; i += blockDim.x) {
+    const int b = i / P.C, c = i - b * P.C;
+    float v = P.b2 ? P.b2[c] : 0.f;
+    for (int t = 0; t < tiles; ++t) {   // tile order
+      const int64_t j = (static_cast<int64_t>(t) * P.B + b) * P.C + c;
+      v += staged ? s_zp[j] : __ldcg(P.zpart + j);
+    }
+    P.z[i] = v;
+    s_z[i] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < P.B) {
+    const int b = threadIdx.x;
+    int best = 0;
+    float bv = -INFINITY;
+    for (int c = 0; c < P.C; ++c)
+      if (s_z[b * P.C + c] > bv) { bv = s_z[b * P.C + c]; best = c; }
+    P.choice[b] = best;
+    P.bsize[b] = P.block - (P.C - 1) / 2 + best;
   }
 }
 
@@ -302,9 +416,15 @@ static void mlp_tc_shape(int V, int H, int n_sm, int* ksteps, int* kps, int* spl
   *splits = (*ksteps + *kps - 1) / *kps;
 }
 
-static bool mlp_tc_ok(int B, int V, int H, int64_t ld, const void* W1) {
-  return B <= 8 && H % kQTile == 0 && (static_cast<int64_t>(H) * 2) % 16 == 0 && aligned(W1, 16) && V >= 1 &&
-         ld >= V;
+// counters (tiles + 1, padded to 256 B) and layer-2 partials (tiles x B x 32) after the partials
+static size_t mlp_cnt_bytes(int H) { return (static_cast<size_t>(H / kQTile + 1) * sizeof(int) + 255) / 256 * 256; }
+static size_t mlp_tail_bytes(int B, int H) {
+  return mlp_cnt_bytes(H) + static_cast<size_t>(H / kQTile) * B * 32 * sizeof(float);
+}
+
+static bool mlp_tc_ok(int B, int V, int H, int64_t ld, const void* W1, const float* b1) {
+  return B <= 8 && H % kQTile == 0 && (static_cast<int64_t>(H) * 2) % 16 == 0 && aligned(W1, 16) &&
+         (!b1 || aligned(b1, 16)) && V >= 1 && ld >= V;
 }
 
 int mlp_slices(int V, int H, int B) {
@@ -331,7 +451,8 @@ TV_API size_t blockpilot_mlp_workspace_size(int B, int V, int H) {
   int ksteps = 0, kps = 0, splits = 0;
   tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
   const size_t Vp = (static_cast<size_t>(V) + 63) / 64 * 64;
-  const size_t tcb = tv::kMlpHdrBytes + 16 * Vp * 2 + static_cast<size_t>(splits) * B * H * sizeof(float);
+  const size_t tcb = tv::kMlpHdrBytes + 16 * Vp * 2 + static_cast<size_t>(splits) * B * H * sizeof(float) +
+                     tv::mlp_tail_bytes(B, H);
   return std::max(simt, tcb);
 }
 
@@ -347,7 +468,7 @@ TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_
   const size_t need = blockpilot_mlp_workspace_size(B, V, H);
   if (!ws || ws_bytes < need || !tv::aligned(ws, 16)) return TV_EWORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (tv::mlp_tc_ok(B, V, H, ld, W1)) {
+  if (tv::mlp_tc_ok(B, V, H, ld, W1, b1)) {
     int ksteps = 0, kps = 0, splits = 0;
     tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
     const int Vp = (V + 63) / 64 * 64;
@@ -361,17 +482,21 @@ TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_
                        static_cast<uint64_t>(H) * 2, 64, tv::kQK) ||
         !tv::mlp_map2d(&P.maps.x, X, static_cast<uint64_t>(V), 16, static_cast<uint64_t>(Vp) * 2, tv::kQK, 16))
       return TV_ECUDA;
-    P.H = H; P.B = B; P.ksteps = ksteps; P.kps = kps; P.part = part; P.err = err;
+    const int tiles = H / tv::kQTile;
+    int* cnt = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + static_cast<size_t>(splits) * B * H * 4);
+    P.H = H; P.B = B; P.C = C; P.block = block; P.ksteps = ksteps; P.kps = kps; P.part = part; P.err = err;
+    P.cnt = cnt;
+    P.zpart = reinterpret_cast<float*>(reinterpret_cast<char*>(cnt) + tv::mlp_cnt_bytes(H));
+    P.b1 = b1; P.W2 = static_cast<const uint16_t*>(W2); P.b2 = b2;
+    P.z = z; P.choice = choice; P.bsize = bsize;
     static const bool attr = cudaFuncSetAttribute(tv::mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   static_cast<int>(tv::kQSmem)) == cudaSuccess;
     if (!attr) return TV_ECUDA;
     int rc = tv::launch_pdl(tv::mlp_x_kernel, dim3((V + 255) / 256), dim3(256), 0, st,
-                            static_cast<const uint16_t*>(last_logits), ld, row_lse, B, V, Vp, X, err);
+                            static_cast<const uint16_t*>(last_logits), ld, row_lse, B, V, Vp, X, err, cnt,
+                            tiles + 1);
     if (rc == TV_OK)
-      rc = tv::launch_pdl(tv::mlp_tc_kernel, dim3(H / tv::kQTile, splits), dim3(tv::kQThreads), tv::kQSmem, st, P);
-    if (rc == TV_OK)
-      rc = tv::launch_pdl(tv::mlp_l2_kernel, dim3(B), dim3(256), 0, st, static_cast<const float*>(part), splits, B,
-                          H, C, b1, static_cast<const uint16_t*>(W2), b2, block, z, choice, bsize);
+      rc = tv::launch_pdl(tv::mlp_tc_kernel, dim3(tiles, splits), dim3(tv::kQThreads), tv::kQSmem, st, P);
     return rc;
   }
   const int n_slice = tv::mlp_slices(V, H, B);

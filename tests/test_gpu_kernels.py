@@ -504,6 +504,36 @@ def test_blockpilot_zero_weights(tv):
     assert np.all(host(z) == 0) and np.all(host(choice) == 0) and np.all(host(bsize) == 13)
 
 
+@pytest.mark.parametrize("B,V,H,C", [(5, 20011, 512, 7), (1, 4099, 256, 32), (8, 150, 256, 3), (12, 3001, 256, 7)])
+def test_blockpilot_mlp_biases_and_workspace_reuse(tv, B, V, H, C):
+    """Biases, ragged request counts, few hidden tiles (many K splits each), a
+    workspace that starts dirty and is reused: the split-K arrival counters
+    must be cleared by the call and leave no state behind.  B = 12 runs the
+    CUDA-core fallback."""
+    rng = np.random.default_rng(B * 1000 + H)
+    logits = synth.bf16_bits((3.0 * rng.standard_normal((B, V))).astype(np.float32))
+    W1 = synth.bf16_bits((0.05 * rng.standard_normal((V, H))).astype(np.float32))
+    W2 = synth.bf16_bits((0.05 * rng.standard_normal((H, C))).astype(np.float32))
+    b1 = (0.01 * rng.standard_normal(H)).astype(np.float32)
+    b2 = (0.01 * rng.standard_normal(C)).astype(np.float32)
+    L = dev(logits)
+    _, _, _, _, lse = tv.vocab_argmax_topk(L, k=0)
+    need = tv.load_library().blockpilot_mlp_workspace_size(B, V, H)
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
+    rz, rchoice, _ = omlp.blockpilot(logits, W1, b1, W2, b2, 16)
+    tol = 1e-4 * np.abs(rz).max() + 1e-6
+    for _ in range(3):
+        z, choice, bsize = tv.blockpilot_mlp(L, lse, dev(W1), dev(W2), b1=dev(b1), b2=dev(b2), block=16, ws=ws)
+        sync()
+        zg = host(z).astype(np.float64)
+        assert np.abs(zg - rz).max() <= tol
+        for r in range(B):
+            srt = np.sort(rz[r])[::-1]
+            if C == 1 or srt[0] - srt[1] > 2 * tol:
+                assert host(choice)[r] == rchoice[r]
+            assert host(bsize)[r] == 16 - (C - 1) // 2 + host(choice)[r]
+
+
 def test_attn_simt_path_on_bf16_in_subprocess(tv):
     """bf16 / head_dim 128 normally runs on the tensor cores; the SIMT kernel
     for the same shapes is checked in a process with TV_ATTN_PATH=simt."""
