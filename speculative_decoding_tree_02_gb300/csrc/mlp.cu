@@ -220,7 +220,10 @@ __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_
   auto empty = [&](int s) { return sb + kQBarOff + 8u * (kQStages + s); };
   const uint32_t done = sb + kQBarOff + 8u * (2 * kQStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kQBarOff + 8 * (2 * kQStages + 1) + 4);
-  griddep_wait();
+  // Warp 0 (the TMA producer) waits for the softmax kernel later, after its
+  // first W1 loads: W1 is an input of the call, and the softmax kernel lets
+  // this grid launch only after its own wait on whatever ran before the call.
+  if (warp != 0) griddep_wait();
   griddep_release();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
@@ -242,9 +245,21 @@ __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_
 
   if (warp == 0) {
     if (lane == 0) {   // ================= TMA producer
-      for (int i = 0; i < n; ++i) {
+      // the first ring's W1 tiles go out while the softmax kernel may still run
+      const int pre = min(n, kQStages);
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t dst = sb + i * kQStageBytes;
+        const int v = (k0 + i) * kQK;
+        mbar_expect_tx(full(i), kQStageBytes);
+        tma_load_2d(dst, &P.maps.w1, ht * kQTile, v, full(i));
+        tma_load_2d(dst + kQAHalf, &P.maps.w1, ht * kQTile + 64, v, full(i));
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(sb + i * kQStageBytes + 2 * kQAHalf, &P.maps.x, (k0 + i) * kQK, 0, full(i));
+      for (int i = pre; i < n; ++i) {
         const int s = i % kQStages;
-        if (i >= kQStages && !mbar_wait(empty(s), ((i / kQStages) - 1) & 1, abort_flag, err, 21)) break;
+        if (!mbar_wait(empty(s), ((i / kQStages) - 1) & 1, abort_flag, err, 21)) break;
         const uint32_t dst = sb + s * kQStageBytes;
         const int v = (k0 + i) * kQK;
         mbar_expect_tx(full(s), kQStageBytes);
@@ -253,6 +268,8 @@ __global__ void __launch_bounds__(kQThreads, kQCtas) mlp_tc_kernel(const __grid_
         tma_load_2d(dst + 2 * kQAHalf, &P.maps.x, v, 0, full(s));
       }
     }
+    __syncwarp();
+    griddep_wait();
   } else if (warp == 1) {
     if (lane == 0) {   // ================= MMA issuer
       // M = 128, N = 16, A MN-major (transpose bit 15), B K-major
