@@ -17,6 +17,8 @@
 //      position and the per-request offsets; one warp per request counts the
 //      lengths (no assumption that the kept set is a prefix).
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "tv_common.cuh"
 
@@ -217,6 +219,173 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
   }
 }
 
+// Cluster form for T <= 2048 (the single-CTA network above is latency-bound:
+// ~11k SM cycles for its 55 stages at T = 1024).  A cluster of 8 CTAs; every
+// CTA forms all T keys (same left-to-right products), then CTA c ranks its
+// eighth of the positions by counting, over all T keys, those that order
+// before it (rank = #{u : key_u < key_t}; keys are distinct).  For each budget
+// the position of rank K (K < T) holds the limit key: its CTA stores it into
+// every CTA's shared memory, and after the cluster barrier a position is kept
+// iff key < limit (all kept when K = T) -- the same set as rank < K.  Each CTA
+// then scans the keep flags of all positions (so it knows the packed slot of
+// its own) and writes the outputs of its positions and of the requests that
+// start in its range.
+constexpr int kDcCl = 8;
+constexpr int kDcClMaxT = 2048;
+
+__device__ __forceinline__ void st_cluster_u64(unsigned long long* p, uint32_t rank, unsigned long long v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+
+__global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1) dcut_cluster_kernel(
+    const float* __restrict__ conf, int B, int D, int n_rho, DcutK ks, float* __restrict__ score,
+    uint8_t* __restrict__ keep, int32_t* __restrict__ keep_len, int32_t* __restrict__ pack_off,
+    int32_t* __restrict__ pack_idx) {
+  __shared__ __align__(16) unsigned long long s_key[kDcClMaxT + 4];
+  __shared__ __align__(16) uint32_t s_hi[kDcClMaxT + 4];   // score words of the keys
+  __shared__ float s_conf[kDcClMaxT];
+  __shared__ int s_part[kDcutThreads];
+  __shared__ unsigned long long s_lim[kDcutMaxRho];
+  __shared__ uint4 s_w[33];
+  uint32_t crank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+  // this CTA has started; the matching wait comes before the first remote store
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  griddep_wait();
+  griddep_release();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = D + 1;
+  const int T = B * N;
+  const int P = (T + kDcCl - 1) / kDcCl;   // positions per CTA (<= 256)
+  const int p0 = min(T, static_cast<int>(crank) * P), p1 = min(T, p0 + P);
+
+  // 1. keys of every position: s[r,j] = ((1 * c[r,0]) * c[r,1]) ... * c[r,j-1] in fp32
+  for (int i = tid; i < B * D; i += kDcutThreads) s_conf[i] = conf[i];
+  __syncthreads();
+  for (int t = tid; t < T; t += kDcutThreads) {
+    const int r = t / N, j = t - r * N;
+    const float* c = s_conf + r * D;
+    float sc = 1.f;
+    for (int i = 0; i < j; ++i) sc = __fmul_rn(sc, c[i]);
+    s_key[t] = (static_cast<unsigned long long>(~__float_as_uint(sc)) << 32) | static_cast<unsigned>(t);
+    s_hi[t] = ~__float_as_uint(sc);
+    if (t >= p0 && t < p1) score[t] = sc;
+  }
+  if (tid < 4) {   // padding: orders after every key
+    s_key[T + tid] = ~0ull;
+    s_hi[T + tid] = ~0u;
+  }
+  __syncthreads();
+
+  // 2. ranks of this CTA's positions: warp = (key sub-range, group of 32
+  //    positions x0 .. x0 + 31).  key_u < key_x compares the score words and
+  //    breaks ties by position, so a group of four keys wholly below x0 needs
+  //    hi_u <= hi_x, one wholly at or above x0 + 32 needs hi_u < hi_x, and
+  //    only groups that meet the warp's own positions take the full compare.
+  const int G = P <= 32 ? 1 : P <= 64 ? 2 : P <= 128 ? 4 : 8;
+  const int SR = 32 / G;
+  {
+    const int g = warp % G, sr = warp / G;
+    const int x0 = p0 + g * 32, x = x0 + lane;
+    const unsigned long long kx = x < p1 ? s_key[x] : 0ull;
+    const uint32_t hx = static_cast<uint32_t>(kx >> 32);
+    const int T4 = (T + 3) & ~3;
+    const int span = ((T4 + SR - 1) / SR + 3) & ~3;
+    const int u0 = min(T4, sr * span), u1 = min(T4, u0 + span);
+    const uint4* hh = reinterpret_cast<const uint4*>(s_hi);
+    int cnt = 0;
+#pragma unroll 4
+    for (int u = u0; u < u1; u += 4) {
+      const uint4 h = hh[u >> 2];
+      if (u + 3 < x0) {
+        cnt += (h.x <= hx) + (h.y <= hx) + (h.z <= hx) + (h.w <= hx);
+      } else if (u >= x0 + 32) {
+        cnt += (h.x < hx) + (h.y < hx) + (h.z < hx) + (h.w < hx);
+      } else {
+        cnt += (s_key[u] < kx) + (s_key[u + 1] < kx) + (s_key[u + 2] < kx) + (s_key[u + 3] < kx);
+      }
+    }
+    s_part[warp * 32 + lane] = cnt;
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster runs
+  if (tid < p1 - p0) {
+    int rank = 0;
+    for (int sr = 0; sr < SR; ++sr) rank += s_part[sr * G * 32 + tid];
+#pragma unroll
+    for (int a = 0; a < kDcutMaxRho; ++a)
+      if (a < n_rho && rank == ks.K[a])   // rank K exists only when K < T
+        for (uint32_t c = 0; c < kDcCl; ++c) st_cluster_u64(&s_lim[a], c, s_key[p0 + tid]);
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+
+  // 3. keep flags of all positions, one scan for every budget, outputs of this CTA's range
+  unsigned long long lim[kDcutMaxRho];
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) lim[a] = (a < n_rho && ks.K[a] < T) ? s_lim[a] : ~0ull;
+  const int per = (T + kDcutThreads - 1) / kDcutThreads;   // consecutive positions per thread (<= 2)
+  const int t0 = tid * per;
+  uint32_t cw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int t = t0 + q;
+    if (q < per && t < T) {
+      const unsigned long long k = s_key[t];
+#pragma unroll
+      for (int a = 0; a < kDcutMaxRho; ++a)
+        if (a < n_rho && k < lim[a]) cw[a >> 1] += (a & 1) ? 0x10000u : 1u;
+    }
+  }
+  uint4 total;
+  const uint4 ex = block_excl_scan4(make_uint4(cw[0], cw[1], cw[2], cw[3]), s_w, &total);
+#pragma unroll
+  for (int a = 0; a < kDcutMaxRho; ++a) {
+    if (a >= n_rho) break;
+    const int tot = half16(total, a);
+    int o = half16(ex, a);
+    uint8_t* kp = keep + static_cast<int64_t>(a) * T;
+    int32_t* pi = pack_idx ? pack_idx + static_cast<int64_t>(a) * T : nullptr;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int t = t0 + q;
+      if (q < per && t < T) {
+        const int f = s_key[t] < lim[a];
+        if (t >= p0 && t < p1) {
+          kp[t] = static_cast<uint8_t>(f);
+          const int r = t / N;
+          if (t == r * N && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + r] = o;
+          if (f && pi) pi[o] = t;
+        }
+        o += f;
+      }
+    }
+    if (crank == 0 && tid == 0 && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + B] = tot;
+    if (pi)
+      for (int q = max(tot, p0) + tid; q < p1; q += kDcutThreads) pi[q] = -1;
+  }
+  // keep_len of the requests that start in this CTA's range: one warp per request
+  const int r0 = (p0 + N - 1) / N, r1 = (p1 + N - 1) / N;
+  for (int r = r0 + warp; r < r1; r += kDcutThreads / 32) {
+    int c[kDcutMaxRho] = {};
+    for (int j = lane; j < N; j += 32) {
+      const unsigned long long k = s_key[r * N + j];
+#pragma unroll
+      for (int a = 0; a < kDcutMaxRho; ++a) c[a] += a < n_rho && k < lim[a];
+    }
+#pragma unroll
+    for (int a = 0; a < kDcutMaxRho; ++a) {
+      if (a < n_rho) {
+        const int sum = __reduce_add_sync(0xffffffffu, c[a]);
+        if (lane == 0) keep_len[static_cast<int64_t>(a) * B + r] = sum;
+      }
+    }
+  }
+}
+
 // Expected tokens per budget: the kept survival probabilities summed exactly
 // in fixed point (each score in [0, 1] rounded to a multiple of 2^-50, sums
 // of at most 8192 terms fit 64 bits), so the result is within 8192 * 2^-51
@@ -271,6 +440,26 @@ __global__ void __launch_bounds__(kRhoThreads) dcut_rho_kernel(const float* __re
 
 }  // namespace tv
 
+// The cluster kernel runs unless clusters of 8 full-size CTAs cannot be
+// scheduled, or TV_DCUT_PATH=sort asks for the single-CTA sorting network
+// (used by the tests to check that path at small T too).
+static bool dcut_cluster_ok() {
+  static const bool ok = [] {
+    const char* e = std::getenv("TV_DCUT_PATH");
+    if (e && std::strcmp(e, "sort") == 0) return false;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(tv::kDcCl);
+    cfg.blockDim = dim3(tv::kDcutThreads);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tv::dcut_cluster_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    return n > 0;
+  }();
+  return ok;
+}
+
 TV_API size_t dcut_select_workspace_size(int B, int D, int n_rho) {
   (void)B; (void)D; (void)n_rho;
   return 0;
@@ -305,6 +494,9 @@ TV_API int dcut_select(const float* conf, int B, int D, const float* rho, int n_
   if (!attr) return TV_ECUDA;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const int Ti = static_cast<int>(T);
+  if (Ti <= tv::kDcClMaxT && dcut_cluster_ok())
+    return tv::launch_pdl(tv::dcut_cluster_kernel, dim3(tv::kDcCl), dim3(tv::kDcutThreads), 0, st, conf, B, D, n_rho,
+                          ks, score, keep, keep_len, pack_off, pack_idx);
   auto kern = Ti <= 1024 ? tv::dcut_kernel<1> : Ti <= 2048 ? tv::dcut_kernel<2> : Ti <= 4096 ? tv::dcut_kernel<4>
                                                                                   : tv::dcut_kernel<8>;
   return tv::launch_pdl(kern, dim3(1), dim3(tv::kDcutThreads), bytes, st, conf, B, D, n_rho, ks, score, keep,

@@ -346,7 +346,7 @@ def test_retrieve_bad_table_entry_flags_error(tv):
 
 # ---------------------------------------------------------------------- D-cut
 @pytest.mark.parametrize("which", ["workload", "ties", "tiny", "t1500", "t4000", "t8192", "d0",
-                                   "rho8", "nonmonotone"])
+                                   "rho8", "nonmonotone", "zeros", "t1005"])
 def test_dcut_select(tv, which):
     rng = np.random.default_rng(len(which))
     beta = lambda b, d: rng.beta(4.0, 1.5, (b, d)).astype(np.float32)
@@ -368,6 +368,11 @@ def test_dcut_select(tv, which):
     elif which == "nonmonotone":   # confidences above 1: kept sets are not prefixes
         conf = rng.uniform(0.0, 2.0, (125, 15)).astype(np.float32)
         rhos = [0.2, 0.5, 0.8]
+    elif which == "zeros":     # exact zero scores (their score word is all ones)
+        conf = np.where(rng.random((60, 12)) < 0.2, 0.0, beta(60, 12)).astype(np.float32)
+        rhos = [0.1, 0.5, 0.9, 1.0]
+    elif which == "t1005":     # ragged: positions per cluster CTA not a multiple of 4
+        conf = beta(67, 14)
     elif which == "ties":
         rng = np.random.default_rng(5)
         conf = rng.choice(np.array([1.0, 0.5, 0.25, 0.75], np.float32), (40, 9))
@@ -383,6 +388,24 @@ def test_dcut_select(tv, which):
     assert np.array_equal(host(kl), rkl)
     assert np.array_equal(host(po), rpo)
     assert np.array_equal(host(pi), rpi)
+
+
+def test_dcut_select_sorting_network_in_subprocess(tv):
+    """Up to 2048 positions run on the cluster kernel; the single-CTA sorting
+    network for the same sizes is checked in a process with TV_DCUT_PATH=sort."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); sys.path.insert(0, '.');"
+        "import test_gpu_kernels as t, speculative_decoding_tree_02_gb300 as tv;"
+        "[t.test_dcut_select(tv, w) for w in ('workload', 'ties', 'tiny', 't1500', 'rho8', 'nonmonotone')];"
+        "print('sort ok')")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, TV_DCUT_PATH="sort")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "sort ok" in r.stdout, r.stderr[-3000:]
 
 
 # ------------------------------------------------------------------ attention
