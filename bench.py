@@ -328,6 +328,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+LAUNCH_REPS = 8    # calls per graph for the launch-bound rows
+KERNEL_REPS = 4    # calls per graph for the per-kernel times of the step
+
+
+def launch_us(torch, gr, stream):
+    """Per-call time of a graph of LAUNCH_REPS calls."""
+    return time_graph(torch, gr, 200, stream) / LAUNCH_REPS * 1e3
+
+
 def time_graph(torch, graphs, n, stream):
     """Average duration of one replay; ``graphs`` (a graph or a list of graphs
     over distinct buffers) are replayed round-robin so that a working set
@@ -344,13 +353,18 @@ def time_graph(torch, graphs, n, stream):
     return s.elapsed_time(e) / n
 
 
-def capture(torch, fn, stream):
+def capture(torch, fn, stream, reps=1):
+    """Graph of ``reps`` consecutive calls of ``fn``.  Replays of a graph
+    complete on a cadence of about 2 us on this part, so a graph of one short
+    kernel times the cadence, not the kernel; several calls per graph (they
+    chain through programmatic launches, as inside the step) amortise it."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         fn()                                   # first call outside the graph (lazy attributes)
     torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=stream):
-        fn()
+        for _ in range(reps):
+            fn()
     torch.cuda.synchronize()
     return g
 
@@ -464,13 +478,15 @@ def measure_rows(tv, torch, pk, stream, only=None):
         tp, tr = tv.best_first_template(60)
         so = (torch.empty(B, dtype=torch.int32, device="cuda"), torch.empty((B, 3), dtype=torch.float32, device="cuda"),
               torch.zeros(1, dtype=torch.int32, device="cuda"))
-        gr = capture(torch, lambda: tv.graft_stage_decide(dp, dc, doff, [0.6, 0.45, 0.2], max_nodes=S, outputs=so), stream)
-        rows["graft_stage_decide[16 trees x 60 nodes]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+        gr = capture(torch, lambda: tv.graft_stage_decide(dp, dc, doff, [0.6, 0.45, 0.2], max_nodes=S, outputs=so),
+                     stream, reps=LAUNCH_REPS)
+        rows["graft_stage_decide[16 trees x 60 nodes]"] = {"us": round(launch_us(torch, gr, stream), 2),
                                                            "bound": "launch"}
         ro = (torch.empty((B, S), dtype=torch.int32, device="cuda"), torch.empty((B, S), dtype=torch.int32, device="cuda"),
               torch.empty(B, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
-        gr = capture(torch, lambda: tv.graft_replace(dp, dt, dc, S, 0.35, 0, adj, tp, tr, outputs=ro), stream)
-        rows["graft_replace[static, 16 trees x 60 slots]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+        gr = capture(torch, lambda: tv.graft_replace(dp, dt, dc, S, 0.35, 0, adj, tp, tr, outputs=ro), stream,
+                     reps=LAUNCH_REPS)
+        rows["graft_replace[static, 16 trees x 60 slots]"] = {"us": round(launch_us(torch, gr, stream), 2),
                                                               "bound": "launch"}
         Bt, St = 64, 17
         tpar = to_dev(np.tile(np.arange(-1, St - 1, dtype=np.int32), Bt), torch)
@@ -479,13 +495,14 @@ def measure_rows(tv, torch, pk, stream, only=None):
         to = (torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
               torch.empty((Bt, St), dtype=torch.int32, device="cuda"),
               torch.empty(Bt, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"))
-        gr = capture(torch, lambda: tv.graft_replace(tpar, ttok, tconf, St, 0.3, 1, adj, tp, tr, outputs=to), stream)
-        rows["graft_replace[TAIL, 64 blocks x 16 drafts]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+        gr = capture(torch, lambda: tv.graft_replace(tpar, ttok, tconf, St, 0.3, 1, adj, tp, tr, outputs=to), stream,
+                     reps=LAUNCH_REPS)
+        rows["graft_replace[TAIL, 64 blocks x 16 drafts]"] = {"us": round(launch_us(torch, gr, stream), 2),
                                                               "bound": "launch"}
         dconf = to_dev(synth.dcut_batch(with_attention=False, with_logits=False)["conf"], torch)
         sc, kp, *_ = tv.dcut_select(dconf, list(synth.DCUT_RHOS))
-        gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream)
-        rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(time_graph(torch, gr, 200, stream) * 1e3, 2),
+        gr = capture(torch, lambda: tv.dcut_choose_rho(sc, kp, [1.0, 1.35, 1.8, 2.4]), stream, reps=LAUNCH_REPS)
+        rows["dcut_choose_rho[bs=64, 4 budgets]"] = {"us": round(launch_us(torch, gr, stream), 2),
                                                       "bound": "launch"}
     # T = 1 verification on the D-cut batch shape: 64 chains of 1 + 15 with
     # target and draft logits at every node (bf16, 151936); one CTA per
@@ -616,8 +633,8 @@ def gpu_arm(args):
     # per-kernel graphs on the same buffers: average launch duration of each kernel
     per_kernel = {}
     for name, f, _ in kernels:
-        gk = capture(torch, f, stream)
-        per_kernel[name] = time_graph(torch, gk, max(5, args.steps // 2), stream)
+        gk = capture(torch, f, stream, reps=KERNEL_REPS)
+        per_kernel[name] = time_graph(torch, gk, max(5, args.steps // 2), stream) / KERNEL_REPS
     a_bytes = attn_bytes(plen, K)           # |keep| = K exactly
     a_ms = per_kernel["tree_verify_attn"]
     traffic = load_traffic("tree_verify_attn", WORKLOAD)

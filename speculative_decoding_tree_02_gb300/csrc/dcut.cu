@@ -248,7 +248,7 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
   __shared__ __align__(16) unsigned long long s_key[kDcClMaxT + 4];
   __shared__ __align__(16) uint32_t s_hi[kDcClMaxT + 4];   // score words of the keys
   __shared__ float s_conf[kDcClMaxT];
-  __shared__ int s_part[kDcutThreads];
+  __shared__ int s_part[2 * kDcutThreads];
   __shared__ unsigned long long s_lim[kDcutMaxRho];
   __shared__ uint4 s_w[33];
   uint32_t crank;
@@ -281,41 +281,50 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
   }
   __syncthreads();
 
-  // 2. ranks of this CTA's positions: warp = (key sub-range, group of 32
-  //    positions x0 .. x0 + 31).  key_u < key_x compares the score words and
-  //    breaks ties by position, so a group of four keys wholly below x0 needs
-  //    hi_u <= hi_x, one wholly at or above x0 + 32 needs hi_u < hi_x, and
-  //    only groups that meet the warp's own positions take the full compare.
-  const int G = P <= 32 ? 1 : P <= 64 ? 2 : P <= 128 ? 4 : 8;
+  // 2. ranks of this CTA's positions.  Warp = (key sub-range, group of 64
+  //    positions x0 .. x0 + 63); lane l ranks x0 + l and x0 + 32 + l.
+  //    key_u < key_x compares the score words and breaks ties by position,
+  //    so keys below x0 need hi_u <= hi_x, keys at or above x0 + 64 need
+  //    hi_u < hi_x, and only the four-key groups that meet the warp's own
+  //    positions take the full 64-bit compare.
+  const int G = P <= 64 ? 1 : P <= 128 ? 2 : 4;
   const int SR = 32 / G;
   {
     const int g = warp % G, sr = warp / G;
-    const int x0 = p0 + g * 32, x = x0 + lane;
-    const unsigned long long kx = x < p1 ? s_key[x] : 0ull;
-    const uint32_t hx = static_cast<uint32_t>(kx >> 32);
+    const int x0 = p0 + g * 64, xa = x0 + lane, xb = xa + 32;
+    const unsigned long long ka = xa < p1 ? s_key[xa] : 0ull, kb = xb < p1 ? s_key[xb] : 0ull;
+    const uint32_t ha = static_cast<uint32_t>(ka >> 32), hb = static_cast<uint32_t>(kb >> 32);
     const int T4 = (T + 3) & ~3;
     const int span = ((T4 + SR - 1) / SR + 3) & ~3;
     const int u0 = min(T4, sr * span), u1 = min(T4, u0 + span);
+    const int m0 = min(max(x0 & ~3, u0), u1), m1 = min(max((x0 + 64 + 3) & ~3, m0), u1);
     const uint4* hh = reinterpret_cast<const uint4*>(s_hi);
-    int cnt = 0;
+    int ca = 0, cb = 0;
 #pragma unroll 4
-    for (int u = u0; u < u1; u += 4) {
+    for (int u = u0; u < m0; u += 4) {   // wholly below x0
       const uint4 h = hh[u >> 2];
-      if (u + 3 < x0) {
-        cnt += (h.x <= hx) + (h.y <= hx) + (h.z <= hx) + (h.w <= hx);
-      } else if (u >= x0 + 32) {
-        cnt += (h.x < hx) + (h.y < hx) + (h.z < hx) + (h.w < hx);
-      } else {
-        cnt += (s_key[u] < kx) + (s_key[u + 1] < kx) + (s_key[u + 2] < kx) + (s_key[u + 3] < kx);
-      }
+      ca += (h.x <= ha) + (h.y <= ha) + (h.z <= ha) + (h.w <= ha);
+      cb += (h.x <= hb) + (h.y <= hb) + (h.z <= hb) + (h.w <= hb);
     }
-    s_part[warp * 32 + lane] = cnt;
+    for (int u = m0; u < m1; ++u) {       // meets x0 .. x0 + 63
+      const unsigned long long k = s_key[u];
+      ca += k < ka;
+      cb += k < kb;
+    }
+#pragma unroll 4
+    for (int u = m1; u < u1; u += 4) {   // wholly at or above x0 + 64
+      const uint4 h = hh[u >> 2];
+      ca += (h.x < ha) + (h.y < ha) + (h.z < ha) + (h.w < ha);
+      cb += (h.x < hb) + (h.y < hb) + (h.z < hb) + (h.w < hb);
+    }
+    s_part[warp * 64 + lane] = ca;
+    s_part[warp * 64 + 32 + lane] = cb;
   }
   __syncthreads();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster runs
   if (tid < p1 - p0) {
     int rank = 0;
-    for (int sr = 0; sr < SR; ++sr) rank += s_part[sr * G * 32 + tid];
+    for (int sr = 0; sr < SR; ++sr) rank += s_part[sr * G * 64 + tid];
 #pragma unroll
     for (int a = 0; a < kDcutMaxRho; ++a)
       if (a < n_rho && rank == ks.K[a])   // rank K exists only when K < T
@@ -329,16 +338,15 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
   for (int a = 0; a < kDcutMaxRho; ++a) lim[a] = (a < n_rho && ks.K[a] < T) ? s_lim[a] : ~0ull;
   const int per = (T + kDcutThreads - 1) / kDcutThreads;   // consecutive positions per thread (<= 2)
   const int t0 = tid * per;
+  unsigned long long kt[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) kt[q] = (q < per && t0 + q < T) ? s_key[t0 + q] : ~0ull;
   uint32_t cw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    const int t = t0 + q;
-    if (q < per && t < T) {
-      const unsigned long long k = s_key[t];
 #pragma unroll
-      for (int a = 0; a < kDcutMaxRho; ++a)
-        if (a < n_rho && k < lim[a]) cw[a >> 1] += (a & 1) ? 0x10000u : 1u;
-    }
+    for (int a = 0; a < kDcutMaxRho; ++a)
+      if (a < n_rho && kt[q] < lim[a]) cw[a >> 1] += (a & 1) ? 0x10000u : 1u;
   }
   uint4 total;
   const uint4 ex = block_excl_scan4(make_uint4(cw[0], cw[1], cw[2], cw[3]), s_w, &total);
@@ -353,7 +361,7 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
     for (int q = 0; q < 2; ++q) {
       const int t = t0 + q;
       if (q < per && t < T) {
-        const int f = s_key[t] < lim[a];
+        const int f = kt[q] < lim[a];
         if (t >= p0 && t < p1) {
           kp[t] = static_cast<uint8_t>(f);
           const int r = t / N;
