@@ -223,22 +223,30 @@ __global__ void __launch_bounds__(kDcutThreads, 1) dcut_kernel(
 // ~11k SM cycles for its 55 stages at T = 1024).  A cluster of 8 CTAs; every
 // CTA forms all T keys (same left-to-right products), then CTA c ranks its
 // eighth of the positions by counting, over all T keys, those that order
-// before it (rank = #{u : key_u < key_t}; keys are distinct).  For each budget
-// the position of rank K (K < T) holds the limit key: its CTA stores it into
-// every CTA's shared memory, and after the cluster barrier a position is kept
-// iff key < limit (all kept when K = T) -- the same set as rank < K.  Each CTA
-// then scans the keep flags of all positions (so it knows the packed slot of
-// its own) and writes the outputs of its positions and of the requests that
-// start in its range.
+// before it (rank = #{u : key_u < key_t}; keys are distinct).  Position t is
+// kept for budget K iff rank(t) < K, so each CTA knows the flags of its own
+// positions at once; it stores its kept counts into every CTA's shared memory,
+// and after one cluster barrier the counts of the CTAs before it give the
+// packed slot of its first kept position.  It writes the outputs of its
+// positions and the lengths of the requests that start in its range (reading
+// the ranks of a request's later positions from the CTAs that hold them).
 constexpr int kDcCl = 8;
 constexpr int kDcClMaxT = 2048;
 
-__device__ __forceinline__ void st_cluster_u64(unsigned long long* p, uint32_t rank, unsigned long long v) {
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                : "=r"(remote)
                : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+  return remote;
+}
+__device__ __forceinline__ void st_cluster_s32(int* p, uint32_t rank, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr(p, rank)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_cluster_s32(const int* p, uint32_t rank) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr(p, rank)) : "memory");
+  return v;
 }
 
 __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1) dcut_cluster_kernel(
@@ -249,8 +257,9 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
   __shared__ __align__(16) uint32_t s_hi[kDcClMaxT + 4];   // score words of the keys
   __shared__ float s_conf[kDcClMaxT];
   __shared__ int s_part[2 * kDcutThreads];
-  __shared__ unsigned long long s_lim[kDcutMaxRho];
-  __shared__ uint4 s_w[33];
+  __shared__ int s_rank[kDcClMaxT / kDcCl];                // ranks of this CTA's positions
+  __shared__ int s_wcnt[kDcClMaxT / kDcCl / 32][kDcutMaxRho];   // kept per warp of the range
+  __shared__ int s_ccnt[kDcCl][kDcutMaxRho];               // kept per CTA (written by each CTA)
   uint32_t crank;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
   // this CTA has started; the matching wait comes before the first remote store
@@ -273,7 +282,6 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
     for (int i = 0; i < j; ++i) sc = __fmul_rn(sc, c[i]);
     s_key[t] = (static_cast<unsigned long long>(~__float_as_uint(sc)) << 32) | static_cast<unsigned>(t);
     s_hi[t] = ~__float_as_uint(sc);
-    if (t >= p0 && t < p1) score[t] = sc;
   }
   if (tid < 4) {   // padding: orders after every key
     s_key[T + tid] = ~0ull;
@@ -321,68 +329,66 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
     s_part[warp * 64 + 32 + lane] = cb;
   }
   __syncthreads();
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster runs
-  if (tid < p1 - p0) {
-    int rank = 0;
-    for (int sr = 0; sr < SR; ++sr) rank += s_part[sr * G * 64 + tid];
+  // 3. kept flags of this CTA's positions (rank < K), kept counts per warp
+  const int li = tid, t = p0 + li;
+  const bool own = li < p1 - p0;
+  int rank = INT32_MAX;
+  if (own) {
+    rank = 0;
+    for (int sr = 0; sr < SR; ++sr) rank += s_part[sr * G * 64 + li];
+    s_rank[li] = rank;
+  }
+  unsigned ball[kDcutMaxRho];
 #pragma unroll
-    for (int a = 0; a < kDcutMaxRho; ++a)
-      if (a < n_rho && rank == ks.K[a])   // rank K exists only when K < T
-        for (uint32_t c = 0; c < kDcCl; ++c) st_cluster_u64(&s_lim[a], c, s_key[p0 + tid]);
+  for (int a = 0; a < kDcutMaxRho; ++a) {
+    ball[a] = __ballot_sync(0xffffffffu, a < n_rho && rank < ks.K[a]);
+    if (lane == 0 && warp * 32 < P) s_wcnt[warp][a] = __popc(ball[a]);
+  }
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster runs
+  if (tid < n_rho) {   // this CTA's kept count of budget tid, into every CTA
+    int c = 0;
+    for (int w = 0; w * 32 < P; ++w) c += s_wcnt[w][tid];
+    for (uint32_t d = 0; d < kDcCl; ++d) st_cluster_s32(&s_ccnt[crank][tid], d, c);
   }
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 
-  // 3. keep flags of all positions, one scan for every budget, outputs of this CTA's range
-  unsigned long long lim[kDcutMaxRho];
+  // 4. outputs of this CTA's positions: score, keep flags, packing
+  if (own) {
+    score[t] = __uint_as_float(~s_hi[t]);
+    const int r = t / N;
+    const bool first = t == r * N;
 #pragma unroll
-  for (int a = 0; a < kDcutMaxRho; ++a) lim[a] = (a < n_rho && ks.K[a] < T) ? s_lim[a] : ~0ull;
-  const int per = (T + kDcutThreads - 1) / kDcutThreads;   // consecutive positions per thread (<= 2)
-  const int t0 = tid * per;
-  unsigned long long kt[2];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) kt[q] = (q < per && t0 + q < T) ? s_key[t0 + q] : ~0ull;
-  uint32_t cw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-#pragma unroll
-    for (int a = 0; a < kDcutMaxRho; ++a)
-      if (a < n_rho && kt[q] < lim[a]) cw[a >> 1] += (a & 1) ? 0x10000u : 1u;
+    for (int a = 0; a < kDcutMaxRho; ++a) {
+      if (a >= n_rho) break;
+      int o = __popc(ball[a] & ((1u << lane) - 1u));   // kept before t: this warp,
+      for (int w = 0; w < warp; ++w) o += s_wcnt[w][a];             // earlier warps of the range,
+      for (uint32_t c = 0; c < crank; ++c) o += s_ccnt[c][a];       // earlier CTAs
+      const bool f = (ball[a] >> lane) & 1u;
+      keep[static_cast<int64_t>(a) * T + t] = static_cast<uint8_t>(f);
+      if (first && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + r] = o;
+      if (f && pack_idx) pack_idx[static_cast<int64_t>(a) * T + o] = t;
+    }
   }
-  uint4 total;
-  const uint4 ex = block_excl_scan4(make_uint4(cw[0], cw[1], cw[2], cw[3]), s_w, &total);
 #pragma unroll
   for (int a = 0; a < kDcutMaxRho; ++a) {
     if (a >= n_rho) break;
-    const int tot = half16(total, a);
-    int o = half16(ex, a);
-    uint8_t* kp = keep + static_cast<int64_t>(a) * T;
-    int32_t* pi = pack_idx ? pack_idx + static_cast<int64_t>(a) * T : nullptr;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int t = t0 + q;
-      if (q < per && t < T) {
-        const int f = kt[q] < lim[a];
-        if (t >= p0 && t < p1) {
-          kp[t] = static_cast<uint8_t>(f);
-          const int r = t / N;
-          if (t == r * N && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + r] = o;
-          if (f && pi) pi[o] = t;
-        }
-        o += f;
-      }
-    }
+    const int tot = min(ks.K[a], T);   // rank < K holds for exactly min(K, T) positions
     if (crank == 0 && tid == 0 && pack_off) pack_off[static_cast<int64_t>(a) * (B + 1) + B] = tot;
-    if (pi)
-      for (int q = max(tot, p0) + tid; q < p1; q += kDcutThreads) pi[q] = -1;
+    if (pack_idx)
+      for (int q = max(tot, p0) + tid; q < p1; q += kDcutThreads) pack_idx[static_cast<int64_t>(a) * T + q] = -1;
   }
-  // keep_len of the requests that start in this CTA's range: one warp per request
+  // keep_len of the requests that start in this CTA's range: one warp per
+  // request; ranks past this CTA's range come from the CTAs that hold them
   const int r0 = (p0 + N - 1) / N, r1 = (p1 + N - 1) / N;
   for (int r = r0 + warp; r < r1; r += kDcutThreads / 32) {
     int c[kDcutMaxRho] = {};
     for (int j = lane; j < N; j += 32) {
-      const unsigned long long k = s_key[r * N + j];
+      const int u = r * N + j;
+      const int ou = u / P;
+      const int rk = ou == static_cast<int>(crank) ? s_rank[u - p0] : ld_cluster_s32(&s_rank[u - ou * P], ou);
 #pragma unroll
-      for (int a = 0; a < kDcutMaxRho; ++a) c[a] += a < n_rho && k < lim[a];
+      for (int a = 0; a < kDcutMaxRho; ++a) c[a] += a < n_rho && rk < ks.K[a];
     }
 #pragma unroll
     for (int a = 0; a < kDcutMaxRho; ++a) {
@@ -392,6 +398,8 @@ __global__ void __cluster_dims__(kDcCl, 1, 1) __launch_bounds__(kDcutThreads, 1)
       }
     }
   }
+  // a request can reach into later CTAs: none may exit while its ranks can be read
+  if (P % N != 0) asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Expected tokens per budget: the kept survival probabilities summed exactly
