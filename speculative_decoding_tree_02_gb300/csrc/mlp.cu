@@ -9,6 +9,9 @@
 // remainders (x_lo = bf16(x - x_hi)), so h = D[., b] + D[., 8 + b] carries x
 // to about 16 mantissa bits.  W1 streams through a TMA ring once (split-K
 // over V across CTAs); its tile is the MN-major A operand, X the K-major B.
+// The same kernel finishes the job: the last K split of each hidden tile
+// reduces the tile's partials and forms its share of layer 2, the last tile
+// adds the shares and takes the argmax.
 //
 // Fallback layer 1 (more requests): a bandwidth-bound GEMV with 8 right-hand sides (the requests):
 // every W1 element is read once and used for 8 FMAs.  Grid (column block of
@@ -17,8 +20,8 @@
 // x = 2^((l - lse) log2 e) in shared memory.  Warps take W1 rows round-robin,
 // lanes own 8 hidden units (one 16-byte load per row), and the 8 warps'
 // partial sums are reduced through shared memory in warp order.  Layer 2,
-// ReLU and the argmax run in one small CTA per request, summing the V-slices
-// in slice order (deterministic).
+// ReLU and the argmax then run in one small CTA per request, summing the
+// V-slices in slice order (deterministic).
 #include <algorithm>
 #include <cstring>
 
