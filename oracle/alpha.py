@@ -44,12 +44,17 @@ def tv_alpha(lp, lq, branch_off=None, mass_tok=None, rows=None):
         alpha_tv[r] = 1.0 - 0.5 * np.abs(p - q).sum()
         if mass_tok is not None:
             p_mass[r] = p[int(mass_tok[r])]
-    prefix = None
-    if branch_off is not None:
-        prefix = np.full(R, np.nan)
-        for b in range(len(branch_off) - 1):
-            run = 1.0
-            for r in range(int(branch_off[b]), int(branch_off[b + 1])):
-                run *= alpha[r]
-                prefix[r] = run
+    prefix = None if branch_off is None else branch_prefix(alpha, branch_off)
     return alpha, alpha_tv, prefix, p_mass
+
+
+def branch_prefix(alpha, branch_off):
+    """Running product of alpha within each branch, in row order (rows
+    outside every branch are NaN)."""
+    prefix = np.full(len(alpha), np.nan)
+    for b in range(len(branch_off) - 1):
+        run = 1.0
+        for r in range(int(branch_off[b]), int(branch_off[b + 1])):
+            run *= alpha[r]
+            prefix[r] = run
+    return prefix

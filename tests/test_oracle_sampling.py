@@ -72,3 +72,44 @@ def test_one_hot_draft_accepts_with_the_target_probability():
         _, _, _, bonus, _, _ = osm.rejection_verify(parent, tok, pl, ql, np.array([0, 2]), np.array([0.0, 0.9]),
                                                  np.array([uf]), 1)
         assert bonus[0] == want
+
+
+def zero_residual_case(V=64):
+    """A root whose target and draft distributions differ only below the
+    rounding of the normaliser: target logits (0, -40), draft (0, -39), the
+    other tokens at -1000 (exp underflows to exactly 0).  Then p(0) = q(0) = 1
+    exactly, p(1) = e^-40 < q(1) = e^-39, so drafting token 1 is rejected
+    with probability 1 - e^-1 and the residual max(0, p - q) is exactly 0
+    (in float64 and in float32 alike).  The scheme is then undefined (0/0);
+    the reading used: continue with the target softmax.  Children of the
+    root: node 1 drafts token 1, node 2 (only in the two-child tree) drafts
+    token 0; node 2's target puts all its mass on token 2."""
+    pl = np.full((3, V), -1000.0)
+    ql = np.full((3, V), -1000.0)
+    pl[0, :2] = (0.0, -40.0)
+    ql[0, :2] = (0.0, -39.0)
+    pl[1:, 2] = 0.0
+    ql[1:, 2] = 0.0
+    return pl, ql
+
+
+def test_zero_residual_continues_with_the_target_softmax():
+    pl, ql = zero_residual_case()
+    # one child, rejected (u = 0.5 > e^-1): the bonus token comes from the
+    # target softmax at the root, (1, e^-40, 0, ...): token 0 for any u < 1
+    for uf in (0.001, 0.5, 0.999):
+        acc, best, _, bonus, trace, finals = osm.rejection_verify(
+            np.array([-1, 0]), np.array([0, 1]), pl[:2], ql[:2], np.array([0, 2]), np.array([0.0, 0.5]),
+            np.array([uf]), 1)
+        assert acc[0] == 0 and best[0] == 0 and bonus[0] == 0
+        assert abs(trace[0][2] - np.exp(-1.0)) < 1e-12
+        assert np.all(np.isfinite(finals[0])) and finals[0][0] == 1.0
+    # two children: after the zero-residual rejection of node 1, node 2
+    # (token 0) meets p'(0) = q(0) = 1 and is accepted whatever its uniform;
+    # the bonus then comes from node 2's target: token 2
+    acc, best, path, bonus, trace, _ = osm.rejection_verify(
+        np.array([-1, 0, 0]), np.array([0, 1, 0]), pl, ql, np.array([0, 3]), np.array([0.0, 0.5, 0.999]),
+        np.array([0.3]), 2)
+    assert acc[0] == 1 and best[0] == 2 and bonus[0] == 2
+    assert list(path[0]) == [0, 2, -1]
+    assert trace[1][2] == 1.0
