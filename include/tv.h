@@ -157,6 +157,14 @@ int tree_verify_attn(const void* q, const void* k_pre, const void* v_pre, const 
  * Outputs (each may be NULL except argmax): argmax int32, topk_idx int32
  *   [*, k], topk_val float [*, k] (the logit values), row_max float,
  *   row_lse float.
+ * Failure: the streaming kernels wait on shared-memory barriers with a bound
+ *   of about 2 s.  If a wait runs out (only possible when the GPU stalls
+ *   for seconds), every reduced row is written as argmax -1, top-k indices
+ *   -1, and NaN for the top-k values, row_max and row_lse, and the first
+ *   int32 of the workspace is nonzero.  The host return value cannot report
+ *   it (the work is asynchronous).
+ * Workspace: vocab_argmax_topk_workspace_size(rows, V, k) bytes, 16-byte
+ *   aligned; contents need not persist between calls.
  * -------------------------------------------------------------------------- */
 size_t vocab_argmax_topk_workspace_size(int rows, int V, int k);
 int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld,
@@ -183,10 +191,14 @@ int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld
  *   - The first call on a device looks up the array's device address (one
  *     runtime query, no allocation); make that first call before any stream
  *     capture on that device.
- *   - All calls share the one array and it keeps the last call's contents
- *     (nothing in it needs to start at zero: each call clears the small
- *     header it uses with an asynchronous memset on the given stream).  Calls that overlap on the GPU
- *     (different streams without ordering) race on it: order them.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: each call on the streaming path
+ *     resets the small header it uses with a one-thread kernel on the given
+ *     stream, and the fallback path (rows that are not 16-byte multiples)
+ *     overwrites every chunk record it later reads.  Calls that overlap on
+ *     the GPU (different streams without ordering) race on it: order them.
+ *   - An expired wait gives the same failure outputs as vocab_argmax_topk
+ *     (argmax -1, NaN values); the caller cannot read the status word here.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * -------------------------------------------------------------------------- */
 #define TV_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -222,6 +222,21 @@ def vocab_argmax_topk_noalloc(logits, argmax, topk_idx=None, topk_val=None, row_
     R, V = logits.shape
     if rows is None:
         rows = row_idx.numel() if row_idx is not None else R
+    # outputs are indexed by source row: they must cover every row read
+    need = rows
+    if row_idx is not None and rows > 0 and not torch.cuda.is_current_stream_capturing():
+        need = int(row_idx[:rows].max().item()) + 1
+    for name, t, dt, cols in (("argmax", argmax, torch.int32, None), ("topk_idx", topk_idx, torch.int32, k),
+                              ("topk_val", topk_val, torch.float32, k), ("row_max", row_max, torch.float32, None),
+                              ("row_lse", row_lse, torch.float32, None)):
+        if t is None:
+            continue
+        if t.dtype != dt or t.device != logits.device:
+            raise ValueError(f"{name} must be a {dt} tensor on {logits.device}")
+        if cols is not None and (t.dim() != 2 or t.shape[1] != cols):
+            raise ValueError(f"{name} must have {cols} columns")
+        if t.shape[0] < need:
+            raise ValueError(f"{name} has {t.shape[0]} rows, the call writes row {need - 1}")
     _check("vocab_argmax_topk_noalloc", load_library().vocab_argmax_topk_noalloc(
         _ptr(logits), _dtype_code(logits), rows, V, logits.stride(0), _ptr(row_idx), k, _ptr(argmax),
         _ptr(topk_idx), _ptr(topk_val), _ptr(row_max), _ptr(row_lse), _stream()))

@@ -735,9 +735,7 @@ template <int LIVE>
 static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long total_prefix, int* err,
                           cudaStream_t st) {
   using L = tc::Lay<LIVE>;
-  static const bool attr_ok = cudaFuncSetAttribute(tc::attn_tc_kernel<LIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(L::kSmemBytes)) == cudaSuccess;
-  if (!attr_ok) return TV_ECUDA;
+  if (!smem_limit(tc::attn_tc_kernel<LIVE>, static_cast<int>(L::kSmemBytes))) return TV_ECUDA;
   tc::TcParams P;
   std::memset(&P, 0, sizeof(P));
   P.a = p;

@@ -499,14 +499,8 @@ TV_API int dcut_select(const float* conf, int B, int D, const float* rho, int n_
     ks.K[a] = static_cast<int>(std::floor(r * static_cast<double>(T) + 0.5));
   }
   const int bytes = tv::kDcutMaxPos * static_cast<int>(sizeof(unsigned long long) + sizeof(int));
-  static const bool attr = [bytes] {
-    bool ok = true;
-    ok &= cudaFuncSetAttribute(tv::dcut_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tv::dcut_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tv::dcut_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tv::dcut_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
-    return ok;
-  }();
+  const bool attr = tv::smem_limit(tv::dcut_kernel<1>, bytes) && tv::smem_limit(tv::dcut_kernel<2>, bytes) &&
+                    tv::smem_limit(tv::dcut_kernel<4>, bytes) && tv::smem_limit(tv::dcut_kernel<8>, bytes);
   if (!attr) return TV_ECUDA;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const int Ti = static_cast<int>(T);

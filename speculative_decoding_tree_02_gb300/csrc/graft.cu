@@ -219,11 +219,8 @@ TV_API int graft_adj_update(int32_t* adj, int V, int k, const int32_t* tok,
       rc = tv::launch_pdl(tv::adj_copy_kernel, dim3(gv), dim3(256), 0, st, adj, V, k, last, topk_idx, topk_ld, vec4);
     return rc;
   }
-  static const int smem = [] {
-    const int bytes = tv::kAdjWarps * tv::kAdjRows * static_cast<int>(sizeof(int32_t));
-    cudaFuncSetAttribute(tv::adj_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    return bytes;
-  }();
+  const int smem = tv::kAdjWarps * tv::kAdjRows * static_cast<int>(sizeof(int32_t));
+  if (!tv::smem_limit(tv::adj_update_kernel, smem)) return TV_ECUDA;
   const int grid = (V + tv::kAdjRows - 1) / tv::kAdjRows;
   return tv::launch_pdl(tv::adj_update_kernel, dim3(grid), dim3(tv::kAdjWarps * 32), smem, st, adj, V, k, tok,
                         topk_idx, topk_ld, valid, n, n_bad, vec4);

@@ -509,9 +509,7 @@ TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_
     P.zpart = reinterpret_cast<float*>(reinterpret_cast<char*>(cnt) + tv::mlp_cnt_bytes(H));
     P.b1 = b1; P.W2 = static_cast<const uint16_t*>(W2); P.b2 = b2;
     P.z = z; P.choice = choice; P.bsize = bsize;
-    static const bool attr = cudaFuncSetAttribute(tv::mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(tv::kQSmem)) == cudaSuccess;
-    if (!attr) return TV_ECUDA;
+    if (!tv::smem_limit(tv::mlp_tc_kernel, static_cast<int>(tv::kQSmem))) return TV_ECUDA;
     int rc = tv::launch_pdl(tv::mlp_x_kernel, dim3((V + 255) / 256), dim3(256), 0, st,
                             static_cast<const uint16_t*>(last_logits), ld, row_lse, B, V, Vp, X, err, cnt,
                             tiles + 1);

@@ -1,5 +1,29 @@
-// Status strings and version of libtreeverify.
+// Status strings, version and per-device launch attributes of libtreeverify.
+#include <mutex>
+#include <set>
+#include <tuple>
+
 #include "tv_common.cuh"
+
+namespace tv {
+
+bool smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;   // (kernel, device, bytes)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  done.insert(key);
+  return true;
+}
+
+}  // namespace tv
 
 TV_API const char* tv_status_str(int status) {
   switch (status) {

@@ -20,6 +20,15 @@ inline int launch_status() {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device, so it is set once per
+// (kernel, device) and remembered; false when the runtime refuses.
+bool smem_limit(const void* kernel, int bytes);
+template <typename... KArgs>
+inline bool smem_limit(void (*kernel)(KArgs...), int bytes) {
+  return smem_limit(reinterpret_cast<const void*>(kernel), bytes);
+}
+
 // Programmatic dependent launch.  Kernels of the verification step are
 // launched with programmatic stream serialization: a kernel's CTAs may be
 // scheduled while the previous kernel in the stream drains.  Each such

@@ -17,6 +17,7 @@
 #include <float.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "tv_common.cuh"
 
@@ -474,10 +475,12 @@ struct StreamHdr {
 };
 constexpr size_t kStreamHdrBytes = 256;
 
-__global__ void stream_hdr_clear_kernel(StreamHdr* hdr) {
+// `status0` is 0 except when the caller's process plants a failure to test
+// the failure path (TV_TEST_VOCAB_STATUS, read on the host).
+__global__ void stream_hdr_clear_kernel(StreamHdr* hdr, int status0) {
   griddep_wait();
   griddep_release();
-  hdr->status = 0;
+  hdr->status = status0;
   hdr->claim = 0;
 }
 
@@ -721,7 +724,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel
     const StreamPart* __restrict__ part, int n_chunks, int rows, const T* __restrict__ logits, int V,
     int64_t ld, const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_val, float* __restrict__ row_max,
-    float* __restrict__ row_lse) {
+    float* __restrict__ row_lse, const StreamHdr* __restrict__ hdr) {
   __shared__ float s_bv[kMergeWarps][kMergeBuf];
   __shared__ int s_bi[kMergeWarps][kMergeBuf];
   griddep_wait();
@@ -731,6 +734,20 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel
   if (row >= rows) return;
   const int src = row_idx ? row_idx[row] : row;
   const int dst = src;
+  if (__ldcg(&hdr->status) != 0) {
+    // a bounded wait of the streaming kernel ran out: its chunk records are
+    // incomplete, so every row reports failure instead of a stale merge
+    if (lane == 0) {
+      argmax[dst] = -1;
+      if (row_max) row_max[dst] = __int_as_float(0x7fc00000);
+      if (LSE && row_lse) row_lse[dst] = __int_as_float(0x7fc00000);
+    }
+    if (k > 0 && lane < k) {
+      if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = -1;
+      if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
   const StreamPart* gp = part + static_cast<int64_t>(row) * n_chunks;
   const T* x = logits + static_cast<int64_t>(src) * ld;
   auto logit = [&](int e) -> float {
@@ -921,10 +938,7 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
   const bool stream_ok = vec_ok && (static_cast<int64_t>(V) * sizeof(T)) % 16 == 0;
   if (stream_ok) {
     constexpr int smem = stream_stages<T>() * stream_chunk_bytes<T>();
-    static const bool attr = cudaFuncSetAttribute(vocab_stream_kernel<T, KMAX, LSE>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  smem) == cudaSuccess;
-    if (!attr) return TV_ECUDA;
+    if (!smem_limit(vocab_stream_kernel<T, KMAX, LSE>, smem)) return TV_ECUDA;
     const int items = rows * n_chunks;
     // Rows in page-locked host memory arrive over the host link, far slower
     // than HBM: a quarter of the SMs keep it busy and leave the rest to
@@ -932,14 +946,18 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
     const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4) : 4 * sm_count_cached());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
     auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
-    int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr);
+    static const int planted = [] {
+      const char* e = std::getenv("TV_TEST_VOCAB_STATUS");
+      return e ? std::atoi(e) : 0;
+    }();
+    int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr, planted);
     if (rc == TV_OK)
       rc = launch_pdl(vocab_stream_kernel<T, KMAX, LSE>, dim3(grid), dim3(kStreamThreads), smem, st, logits, V, ld,
                       row_idx, rows, n_chunks, sp, hdr);
     if (rc == TV_OK)
       rc = launch_pdl(vocab_stream_merge_kernel<T, KMAX, LSE>, dim3((rows + kMergeWarps - 1) / kMergeWarps),
                       dim3(32 * kMergeWarps), 0, st, sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax,
-                      topk_idx, topk_val, row_max, row_lse);
+                      topk_idx, topk_val, row_max, row_lse, hdr);
     return rc;
   }
   dim3 g1(n_chunks, rows);

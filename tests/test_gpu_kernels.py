@@ -169,18 +169,19 @@ def test_vocab_host_resident_rows(tv, dtype):
     assert np.abs(host(rl)[idx].astype(np.float64) - rrl).max() <= LSE_ATOL
 
 
-def test_vocab_full_size_sample(tv):
-    # the D-cut workload at rho = 1: 1024 rows x 151936, checked on a row sample
+def test_vocab_full_size_every_row(tv):
+    # the D-cut workload at rho = 1: 1024 rows x 151936, every output compared
     d = synth.dcut_batch(with_attention=False)
     L = dev(d["logits"])
     am, ti, tvl, rm, rl = tv.vocab_argmax_topk(L, k=8)
     sync()
     assert np.array_equal(host(am), d["planted"])
-    sel = np.arange(0, 1024, 37)
-    ram, rti, rtv, rrm, rrl = ovoc.argmax_topk(d["logits"], 8, rows=sel)
-    assert np.array_equal(host(ti)[sel], rti)
-    assert np.array_equal(host(tvl)[sel], rtv)
-    assert np.abs(host(rl)[sel] - rrl).max() <= LSE_ATOL
+    ram, rti, rtv, rrm, rrl = ovoc.argmax_topk(d["logits"], 8)
+    assert np.array_equal(host(am), ram)
+    assert np.array_equal(host(ti), rti)
+    assert np.array_equal(host(tvl), rtv)
+    assert np.array_equal(host(rm), rrm)
+    assert np.abs(host(rl) - rrl).max() <= LSE_ATOL
 
 
 # ---------------------------------------------------------------------- alpha
@@ -216,13 +217,22 @@ def test_alpha_identity_is_one(tv):
     np.testing.assert_allclose(a, 1.0, rtol=ALPHA_RTOL)
 
 
-def test_alpha_full_size_sample(tv):
+def test_alpha_full_size_every_row(tv):
+    # the SpecOPD scoring shape: 1024 rows x 151936, p and q; every row's
+    # alpha and softmax mass, and every branch's running product
+    from oracle_pool import OraclePool, alpha_task, split
     d = synth.specopd_tree(with_attention=False)
-    a, pre = check_alpha(tv, d, rows=list(range(0, 1024, 41)))
-    # running product against the oracle's prefix product of the GPU-free alphas
-    ra, _, rpre, _ = oal.tv_alpha(d["lp"][:48], d["lq"][:48], d["branch_off"][:4], None)
-    np.testing.assert_allclose(pre[:48], rpre, rtol=ALPHA_RTOL)
-    assert np.all(np.diff(pre.reshape(64, 16), axis=1) <= 0)
+    a, pre, pm = tv.tree_tv_alpha(dev(d["lp"]), dev(d["lq"]), dev(d["branch_off"]), dev(d["mass_tok"]))
+    sync()
+    ra = np.full(1024, np.nan)
+    rpm = np.full(1024, np.nan)
+    with OraclePool({"lp": d["lp"], "lq": d["lq"], "mass_tok": d["mass_tok"]}) as pool:
+        for rows, a_r, pm_r in pool.map(alpha_task, split(range(1024), 64)):
+            ra[rows], rpm[rows] = a_r, pm_r
+    np.testing.assert_allclose(host(a), ra, rtol=ALPHA_RTOL)
+    np.testing.assert_allclose(host(pm), rpm, rtol=ALPHA_RTOL)
+    np.testing.assert_allclose(host(pre), oal.branch_prefix(ra, d["branch_off"]), rtol=ALPHA_RTOL)
+    assert np.all(np.diff(host(pre).reshape(64, 16), axis=1) <= 0)
 
 
 # ----------------------------------------------------------------- acceptance
@@ -455,23 +465,42 @@ def test_attn_dcut_small_with_node_cnt(tv):
     run_attn(tv, d, node_cnt=cnt)
 
 
-def test_attn_dcut_full_size_sample(tv):
-    d = synth.dcut_batch(with_logits=False)
-    sel = [r * 16 + j for r in (0, 17, 40, 63) for j in (0, 7, 15)]
-    run_attn(tv, d, nodes=sel)
+def run_attn_full(tv, d, node_cnt=None):
+    """Every output of a full-size workload against the oracle."""
+    off, pre_off = d["node_off"], d["pre_off"]
+    sizes = np.diff(off)
+    max_nodes, max_prefix = int(sizes.max()), int(np.diff(pre_off).max())
+    plen = np.diff(pre_off).astype(np.int32)
+    _, _, anc, _, _ = tv.tv_tree_prep(dev(d["parent"]), dev(off), dev(plen), dev(d["vis_prefix"]), max_nodes,
+                                      (max_nodes + 63) // 64)
+    o, lse = tv.tree_verify_attn(dev(d["q"]), dev(d["k_pre"]), dev(d["v_pre"]), dev(pre_off), dev(d["k_tree"]),
+                                 dev(d["v_tree"]), dev(off), anc, max_nodes, max_prefix,
+                                 vis_prefix=dev(d["vis_prefix"]), node_cnt=dev(node_cnt))
+    sync()
+    from oracle_pool import oracle_attention_all
+    ro, rlse = oracle_attention_all(d, node_cnt)
+    got = out_to_f64(o)
+    ok, err, scale = attn_close(got, ro, ATTN_BF16)
+    assert ok, (err, scale)
+    m = ~np.isnan(rlse)
+    assert np.abs(host(lse)[m] - rlse[m]).max() <= 1e-4
+    return got, ro
 
 
-def test_attn_blockpilot_sample(tv):
-    d = synth.blockpilot_sweep(with_mlp=False, V=64)
-    N = d["nodes_per_request"]
-    sel = [r * N + j for r in (0, 7) for j in (0, 1, 13, 14, 112)]
-    run_attn(tv, d, nodes=sel)
+def test_attn_dcut_full_size_every_node(tv):
+    # 64 requests x 16 nodes, prefixes 512..4096: every node and head
+    run_attn_full(tv, synth.dcut_batch(with_logits=False))
 
 
-def test_attn_specopd_sample(tv):
-    d = synth.specopd_tree(with_logits=False)
-    sel = list(range(0, 16)) + [16 * 31 + 3, 16 * 63 + 15, 16 * 40]
-    run_attn(tv, d, nodes=sel)
+def test_attn_blockpilot_full_size_every_node(tv):
+    # 8 requests x 113 nodes over 8192-token prefixes (the 64-row / 128-row
+    # tensor-core tiles and their ragged last tile)
+    run_attn_full(tv, synth.blockpilot_sweep(with_mlp=False, V=64))
+
+
+def test_attn_specopd_full_size_every_node(tv):
+    # 1024 branch nodes over one 4096-token trunk: all 32 128-row tiles
+    run_attn_full(tv, synth.specopd_tree(with_logits=False))
 
 
 def test_attn_edge_cases(tv):
@@ -591,3 +620,59 @@ def test_attn_status_word_clear(tv):
                         dev(d["v_tree"]), dev(off), anc, 16, int(plen.max()), ws=ws)
     sync()
     assert int(ws[:4].view(torch.int32).item()) == 0
+
+
+def test_host_validation_with_real_buffers(tv):
+    """The calls the host-side checks must refuse, given a real 64 MB device
+    buffer for every array argument (large enough for any launch these
+    argument lists could describe), so a validation regression could not
+    reach memory outside it."""
+    import ctypes
+    import test_host_abi as tha
+    buf = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    for want, call in tha.validation_calls(tv.load_library(), ctypes.c_void_p(buf.data_ptr())):
+        assert call() == want
+    torch.cuda.synchronize()
+    assert int(buf.count_nonzero()) == 0                  # nothing ran
+
+
+def test_vocab_expired_wait_reports_failure_in_subprocess(tv):
+    """When a bounded wait of the streaming kernels runs out, every reduced row
+    reports failure (argmax -1, NaN values) and the workspace status word is
+    nonzero, instead of a merge of stale chunk records.  The failure is planted
+    on the host (TV_TEST_VOCAB_STATUS sets the status word where the call
+    would clear it), so no wait actually runs out and nothing faults."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); sys.path.insert(0, '.');"
+        "import numpy as np, torch, synth, speculative_decoding_tree_02_gb300 as tv;"
+        "x = synth.bf16_bits(np.random.default_rng(1).standard_normal((5, 40000)).astype(np.float32));"
+        "L = torch.from_numpy(x.view(np.int16)).cuda();"
+        "ws = torch.zeros(tv.load_library().vocab_argmax_topk_workspace_size(5, 40000, 8), dtype=torch.uint8,"
+        " device='cuda');"
+        "am, ti, tvl, rm, rl = tv.vocab_argmax_topk(L, k=8, ws=ws); torch.cuda.synchronize();"
+        "assert (am == -1).all() and (ti == -1).all() and torch.isnan(tvl).all();"
+        "assert torch.isnan(rm).all() and torch.isnan(rl).all();"
+        "assert int(ws[:4].view(torch.int32).item()) == 3;"
+        "o = (torch.zeros(5, dtype=torch.int32, device='cuda'), torch.zeros((5, 8), dtype=torch.int32, device='cuda'),"
+        " torch.zeros((5, 8), device='cuda'), torch.zeros(5, device='cuda'), torch.zeros(5, device='cuda'));"
+        "tv.vocab_argmax_topk_noalloc(L, *o, k=8); torch.cuda.synchronize();"
+        "assert (o[0] == -1).all() and torch.isnan(o[4]).all();"
+        "print('failure reported')")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, TV_TEST_VOCAB_STATUS="3")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "failure reported" in r.stdout, r.stderr[-3000:]
+
+
+def test_vocab_status_word_clear_after_a_normal_call(tv):
+    x = synth.bf16_bits(np.random.default_rng(2).standard_normal((5, 40000)).astype(np.float32))
+    ws = torch.full((tv.load_library().vocab_argmax_topk_workspace_size(5, 40000, 8),), 7, dtype=torch.uint8,
+                    device="cuda")
+    am = tv.vocab_argmax_topk(dev(x), k=8, ws=ws)[0]
+    sync()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert np.array_equal(host(am), ovoc.argmax_topk(x, 1)[0])

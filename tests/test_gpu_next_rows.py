@@ -236,3 +236,30 @@ def test_rejection_sampling_identical_distributions(tv):
                 break
             cur, d = kids[0], d + 1
         assert host(acc)[r] == d and host(best)[r] == cur
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rejection_sampling_zero_residual(tv, dtype):
+    # the hand-built case of the oracle's pin: a rejection whose residual
+    # max(0, p - q) is exactly 0 (float32 as well) continues with the
+    # target softmax, on the GPU as in the oracle
+    import test_oracle_sampling as tos
+    from oracle import sampling as osm
+    pl, ql = tos.zero_residual_case()
+    conv = (lambda x: synth.bf16_bits(x.astype(np.float32))) if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    for parent, tok, u in (([-1, 0], [0, 1], [0.0, 0.5]), ([-1, 0, 0], [0, 1, 0], [0.0, 0.5, 0.999])):
+        n = len(parent)
+        par, tk = np.array(parent, np.int32), np.array(tok, np.int32)
+        un = np.array(u, np.float32)
+        for uf in (0.001, 0.3, 0.999):
+            ufa = np.array([uf], np.float32)
+            off = np.array([0, n], np.int32)
+            acc, best, path, bonus = tv.accept_rejection_sampling(dev(par), dev(tk), dev(conv(pl[:n])),
+                                                                  dev(conv(ql[:n])), dev(off), dev(un), dev(ufa),
+                                                                  max_depth=n - 1)
+            sync()
+            racc, rbest, rpath, rbonus, _, _ = osm.rejection_verify(par, tk, conv(pl[:n]), conv(ql[:n]), off, un,
+                                                                    ufa, n - 1)
+            assert host(acc)[0] == racc[0] and host(best)[0] == rbest[0] and host(bonus)[0] == rbonus[0]
+            assert np.array_equal(host(path), rpath)
+            assert rbonus[0] == (0 if n == 2 else 2)

@@ -4,16 +4,21 @@ Callers such as runtimes with a fixed, pre-planned device-memory budget, or
 serving loops whose allocator forbids cudaMalloc on the hot path, cannot hand
 the library a workspace.  This entry point keeps its scratch in a fixed
 device array inside the library.  Checked here through the C ABI against the
-workspace-taking entry point, on two calls in a row (the scratch keeps the
-previous call's contents).  The file is named to be collected last.
+workspace-taking entry point and against the oracle, on two calls in a row
+(the scratch keeps the previous call's contents), on both of its internal
+paths (streamed chunks; the fallback for rows that are not 16-byte
+multiples).  The file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
+from oracle import vocab as ovoc
 
 pytestmark = pytest.mark.gpu
+
+LSE_ATOL = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -33,40 +38,63 @@ def outputs(R, k, dev="cuda"):
             torch.zeros(R, dtype=torch.float32, device=dev))
 
 
+def against_oracle(host_logits, got, k, rows=None):
+    sel = np.arange(host_logits.shape[0]) if rows is None else rows
+    ram, rti, rtv, rrm, rrl = ovoc.argmax_topk(host_logits, k, rows=sel)
+    am, ti, tvl, rm, rl = (t.cpu().numpy() for t in got)
+    assert np.array_equal(am[sel], ram)
+    assert np.array_equal(ti[sel], rti) and np.array_equal(tvl[sel], rtv)
+    assert np.array_equal(rm[sel], rrm)
+    assert np.abs(rl[sel].astype(np.float64) - rrl).max() <= LSE_ATOL
+
+
+# (61, 151936, bf16): the Graft single-request rows; (300, 20000, bf16, k=16);
+# (60, 1000, f32) and (7, 1001, f32): rows of 1001 floats are not 16-byte
+# multiples, so that call takes the fallback kernels and their records
 @pytest.mark.parametrize("rows,V,k,dtype", [(61, synth.QWEN3_VOCAB, 8, "bf16"), (300, 20000, 16, "bf16"),
-                                            (60, 1000, 8, "f32")])
-def test_noalloc_matches_workspace_entry_point_twice(tv, rows, V, k, dtype):
+                                            (60, 1000, 8, "f32"), (7, 1001, 8, "f32")])
+def test_noalloc_matches_workspace_entry_point_and_oracle_twice(tv, rows, V, k, dtype):
     for call in range(2):
         rng = np.random.default_rng(100 * call + rows)
         x = (rng.standard_normal((rows, V)) * 2).astype(np.float32)
-        host = synth.bf16_bits(x).view(np.int16) if dtype == "bf16" else x
-        L = torch.from_numpy(host).cuda()
+        host = synth.bf16_bits(x) if dtype == "bf16" else x
+        L = torch.from_numpy(host.view(np.int16) if dtype == "bf16" else host).cuda()
         ref = tv.vocab_argmax_topk(L, k=k)
         got = tv.vocab_argmax_topk_noalloc(L, *outputs(rows, k), k=k)
         torch.cuda.synchronize()
         for a, b in zip(ref[:4], got[:4]):
             assert torch.equal(a, b)                       # integer results and max: bit-exact
-        assert torch.allclose(ref[4], got[4], rtol=0, atol=1e-5)
+        assert torch.allclose(ref[4], got[4], rtol=0, atol=LSE_ATOL)
+        against_oracle(host, got, k)
 
 
 def test_noalloc_row_gather(tv):
     d = synth.dcut_batch(B=5, V=12000, with_attention=False)
     L = torch.from_numpy(d["logits"].view(np.int16)).cuda()
-    idx = torch.tensor([3, 9, 40, 77, 79], dtype=torch.int32, device="cuda")
-    ref = tv.vocab_argmax_topk(L, k=8, row_idx=idx, out_rows=80)
-    got = tv.vocab_argmax_topk_noalloc(L, *outputs(80, 8), k=8, row_idx=idx)
+    idx = np.array([3, 9, 40, 77, 79], np.int32)
+    ref = tv.vocab_argmax_topk(L, k=8, row_idx=torch.from_numpy(idx).cuda(), out_rows=80)
+    got = tv.vocab_argmax_topk_noalloc(L, *outputs(80, 8), k=8, row_idx=torch.from_numpy(idx).cuda())
     torch.cuda.synchronize()
-    sel = idx.long()
+    sel = torch.from_numpy(idx).long().cuda()
     for a, b in zip(ref[:4], got[:4]):
         assert torch.equal(a[sel], b[sel])
+    against_oracle(d["logits"], got, 8, rows=idx)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(tv):
-    import ctypes
+    # the first row count whose scratch need exceeds the fixed array; the
+    # buffers are real and sized for the call, and the entry point must
+    # refuse it on the host (TV_EWORKSPACE) before any launch
     lib = tv.load_library()
-    need = lib.vocab_argmax_topk_workspace_size(20000, synth.QWEN3_VOCAB, 8)
-    assert need > (32 << 20)
-    status = lib.vocab_argmax_topk_noalloc(ctypes.c_void_p(256), 1, 20000, synth.QWEN3_VOCAB,
-                                           synth.QWEN3_VOCAB, None, 8, ctypes.c_void_p(256),
-                                           ctypes.c_void_p(256), None, None, None, None)
-    assert status == -4                                   # TV_EWORKSPACE, nothing launched
+    V, k = synth.QWEN3_VOCAB, 8
+    rows = 1
+    while lib.vocab_argmax_topk_workspace_size(rows, V, k) <= (32 << 20):
+        rows += 1
+    assert rows == 1699
+    L = torch.zeros((rows, V), dtype=torch.bfloat16, device="cuda")
+    am, ti, tvl, rm, rl = outputs(rows, k)
+    with pytest.raises(tv.TVError) as e:
+        tv.vocab_argmax_topk_noalloc(L, am, ti, tvl, rm, rl, k=k)
+    assert e.value.status == -4
+    torch.cuda.synchronize()
+    assert bool((am == -1).all())                         # nothing was written
