@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import json
 import math
+import re
 import multiprocessing as mp
 import os
 import statistics
@@ -130,7 +131,7 @@ def oracle_step(d, reqs, pool, rho, adj, tmpl):
     return nodes
 
 
-def run_cpu_oracle(d, rho, steps, warmup):
+def run_cpu_oracle(d, rho, steps, warmup, cores=None):
     """Time the oracle: W + K steps, each on the kept positions of cores / 8
     requests (7 i mod B for the i-th request taken).  Returns (nodes/s,
     cores, sample text, sec/step)."""
@@ -138,7 +139,8 @@ def run_cpu_oracle(d, rho, steps, warmup):
     from oracle import graft as ogr
     tmpl = ogr.stage_templates()
     adj = synth.successor_table(3)
-    cores = max(1, min(os.cpu_count() or 1, 16))
+    if cores is None:
+        cores = max(1, min(os.cpu_count() or 1, 16))
     saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     for k in saved:
         os.environ[k] = "1"
@@ -569,6 +571,264 @@ def large_tree_row(tv, torch, d, pk, stream):
             "bound": "tensor", "bytes": byts, "gbs": round(byts / us / 1e3, 1)}
 
 
+# ============================================================ per-config steps
+def _step_row(torch, stream, sets, make, nodes, byts, pk, note):
+    """Time one verification step of a workload.  ``sets``: input sets
+    (rotated so that repeats are not served from L2); ``make(set)`` returns
+    (step_fn, [(kernel name, fn, launches)]).  Reports the step time, verified
+    nodes per second, the step's algorithmic bytes against HBM, and each
+    kernel's time as a graph of KERNEL_REPS consecutive calls."""
+    made = [make(t) for t in sets]
+    grs = [capture(torch, m[0], stream) for m in made]
+    us = time_graph(torch, grs, max(50, 10 * len(grs)), stream) * 1e3
+    kern = {}
+    for name, fn, _ in made[0][1]:
+        gk = capture(torch, fn, stream, reps=KERNEL_REPS)
+        kern[name] = round(time_graph(torch, gk, 50, stream) / KERNEL_REPS * 1e3, 2)
+    return {"us": round(us, 2), "nodes": nodes, "nodes_per_s": round(nodes / us * 1e6, 1),
+            "bytes": int(byts), "gbs": round(byts / us / 1e3, 1), "frac_hbm": round(byts / us / 1e3 / pk["hbm"], 3),
+            "launches": sum(n for _, _, n in made[0][1]), "kernels_us": kern, "step": note}
+
+
+def config_steps(tv, torch, pk, stream):
+    """One verification step of each of the other four workloads, as CUDA
+    graphs (the D-cut batch is the headline line itself)."""
+    rows = {}
+    i32 = lambda *s: torch.empty(s, dtype=torch.int32, device="cuda")
+    V = synth.QWEN3_VOCAB
+    lib = tv.load_library()
+
+    def attn_call(t, n_nodes, max_nodes, max_prefix, B, Hq, Hkv, d, dt, vis=None, want_lse=False):
+        ws = torch.empty(max(256, lib.tree_verify_attn_workspace_size(B, max_nodes, max_prefix, Hq, Hkv, d, dt)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(t["q"])
+        return lambda: tv.tree_verify_attn(t["q"], t["k_pre"], t["v_pre"], t["pre_off"], t["k_tree"], t["v_tree"],
+                                           t["node_off"], t["anc"], max_nodes, max_prefix, vis_prefix=vis, out=out,
+                                           want_lse=want_lse, ws=ws)
+
+    def dev_set(d, keys):
+        return {k: to_dev(d[k], torch) for k in keys}
+
+    # ---- workload 1: tiny tree (V = 1000, prefix 128, 60 nodes, fp32, 4/1 heads, d = 64)
+    d = synth.tiny_tree()
+    n, P = d["parent"].size, int(d["pre_off"][1])
+    keys = ("q", "k_pre", "v_pre", "k_tree", "v_tree", "logits", "parent", "tok", "adj", "node_off", "pre_off")
+    one = sum(np.asarray(d[k]).nbytes for k in keys)
+
+    def make1(t):
+        t["plen"] = to_dev(np.array([P], np.int32), torch)
+        prep_o = (i32(n), i32(n), torch.empty((n, 1), dtype=torch.int64, device="cuda"), i32(n),
+                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+        t["anc"] = prep_o[2]
+        attn = attn_call(t, n, n, P, 1, 4, 1, 64, 0)
+        voc = (i32(n), i32(n, 8), torch.empty((n, 8), dtype=torch.float32, device="cuda"), None, None)
+        wsv = torch.empty(lib.vocab_argmax_topk_workspace_size(n, 1000, 8), dtype=torch.uint8, device="cuda")
+        acc = (i32(1), i32(1), i32(1, n), i32(1), None)
+        nb = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ks = [("tv_tree_prep", lambda: tv.tv_tree_prep(t["parent"], t["node_off"], t["plen"], None, n, 1, outputs=prep_o), 1),
+              ("tree_verify_attn", attn, 1),
+              ("vocab_argmax_topk", lambda: tv.vocab_argmax_topk(t["logits"], k=8, want_lse=False, want_max=False,
+                                                                  ws=wsv, outputs=voc), 3),
+              ("accept_longest_path", lambda: tv.accept_longest_path(t["parent"], t["tok"], voc[0], t["node_off"],
+                                                                     max_nodes=n, want_path_acc=False, outputs=acc), 1),
+              ("graft_adj_update", lambda: tv.graft_adj_update(t["adj"], t["tok"], voc[1], n_bad=nb), 1)]
+
+        def step():
+            for _, f, _ in ks:
+                f()
+        return step, ks
+    sets = [dev_set(d, keys) for _ in range(copies_for(one))]
+    rows["step[tiny tree: 60 nodes, prefix 128, fp32 4/1 heads d=64, V=1000]"] = _step_row(
+        torch, stream, sets, make1, n, one, pk, "tv_tree_prep -> tree_verify_attn (CUDA cores) -> vocab_argmax_topk "
+        "-> accept_longest_path -> graft_adj_update")
+
+    # ---- workload 2: Graft single request (61 nodes, prefix 2048, V = 151936, table carried)
+    st = synth.graft_static()
+    d = synth.graft_step(0, st)
+    tp, tr, toff = tv.stage_templates()
+    stage, nd, N = d["stage"], d["n_draft"], d["N"]
+    tmpl = [to_dev(x, torch) for x in (tp, tr, toff)]
+    parent = tv.assemble_hybrid(d["parent_draft"], tp[toff[stage]:toff[stage + 1]])
+    adj = to_dev(st["adj0"], torch)
+    # the target's logits for the tokens the first retrieval produces (fixed input)
+    rt0 = tv.graft_retrieve(adj, to_dev(np.array([d["root_tok"]], np.int32), torch),
+                            to_dev(np.array([stage], np.int32), torch), *tmpl, 52)[0]
+    tok0 = np.concatenate([d["tok_draft"], rt0.cpu().numpy()[0, :N - 1 - nd]]).astype(np.int32)
+    d["logits"], _ = synth.graft_logits(d, st, tok0)
+    d["parent"] = parent
+    keys = ("q", "k_pre", "v_pre", "k_tree", "v_tree", "logits", "parent", "node_off", "pre_off")
+    one = sum(np.asarray(d[k]).nbytes for k in keys)
+    root = to_dev(np.array([d["root_tok"]], np.int32), torch)
+    stg = to_dev(np.array([stage], np.int32), torch)
+
+    def make2(t):
+        tokbuf = torch.zeros(1 + nd + 52, dtype=torch.int32, device="cuda")
+        tokbuf[:1 + nd] = to_dev(d["tok_draft"], torch)
+        tok = tokbuf[:N]
+        rtok = tokbuf[1 + nd:].view(1, 52)
+        retr = (rtok, i32(1, 52), i32(1), torch.zeros(1, dtype=torch.int32, device="cuda"))
+        t["plen"] = to_dev(np.array([2048], np.int32), torch)
+        prep_o = (i32(N), i32(N), torch.empty((N, 1), dtype=torch.int64, device="cuda"), i32(N),
+                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+        t["anc"] = prep_o[2]
+        attn = attn_call(t, N, N, 2048, 1, 32, 8, 128, 1)
+        voc = (i32(N), i32(N, 8), torch.empty((N, 8), dtype=torch.float32, device="cuda"), None, None)
+        wsv = torch.empty(lib.vocab_argmax_topk_workspace_size(N, V, 8), dtype=torch.uint8, device="cuda")
+        acc = (i32(1), i32(1), i32(1, 9), i32(1), None)
+        nb = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ks = [("graft_retrieve", lambda: tv.graft_retrieve(adj, root, stg, *tmpl, 52, out=retr), 1),
+              ("tv_tree_prep", lambda: tv.tv_tree_prep(t["parent"], t["node_off"], t["plen"], None, N, 1,
+                                                       outputs=prep_o), 1),
+              ("tree_verify_attn", attn, 2),
+              ("vocab_argmax_topk", lambda: tv.vocab_argmax_topk(t["logits"], k=8, want_lse=False, want_max=False,
+                                                                  ws=wsv, outputs=voc), 3),
+              ("accept_longest_path", lambda: tv.accept_longest_path(t["parent"], tok, voc[0], t["node_off"],
+                                                                     max_nodes=N, max_depth=8, want_path_acc=False,
+                                                                     outputs=acc), 1),
+              ("graft_adj_update", lambda: tv.graft_adj_update(adj, tok, voc[1], n_bad=nb), 1)]
+
+        def step():
+            for _, f, _ in ks:
+                f()
+        return step, ks
+    sets = [dev_set(d, keys) for _ in range(copies_for(one))]
+    rows[f"step[graft: 61 nodes (stage {stage}), prefix 2048, 32/8 heads bf16, V=151936, table 151936x8]"] = _step_row(
+        torch, stream, sets, make2, N, one + 52 * 4 + N * 8 * 4 * 2, pk,
+        "graft_retrieve -> tv_tree_prep -> tree_verify_attn -> vocab_argmax_topk -> accept_longest_path -> "
+        "graft_adj_update (the table carries from step to step)")
+    del sets
+
+    # ---- workload 4: BlockPilot sweep (8 x 113 nodes, prefix 8192, 7 block sizes)
+    d = synth.blockpilot_sweep(with_mlp=False)
+    n, Nr = d["parent"].size, d["nodes_per_request"]
+    keys = ("q", "k_pre", "v_pre", "k_tree", "v_tree", "logits", "parent", "tok", "node_off", "pre_off")
+    one = sum(np.asarray(d[k]).nbytes for k in keys)
+
+    def make4(t):
+        t["plen"] = to_dev(np.full(8, 8192, np.int32), torch)
+        prep_o = (i32(n), i32(n), torch.empty((n, 2), dtype=torch.int64, device="cuda"), i32(n),
+                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+        t["anc"] = prep_o[2]
+        attn = attn_call(t, n, Nr, 8192, 8, 32, 8, 128, 1)
+        voc = (i32(n), None, None, None, None)
+        wsv = torch.empty(lib.vocab_argmax_topk_workspace_size(n, V, 0), dtype=torch.uint8, device="cuda")
+        acc = (i32(8), i32(8), i32(8, 20), i32(8), i32(n))
+        ks = [("tv_tree_prep", lambda: tv.tv_tree_prep(t["parent"], t["node_off"], t["plen"], None, Nr, 2,
+                                                       outputs=prep_o), 1),
+              ("tree_verify_attn", attn, 2),
+              ("vocab_argmax_topk", lambda: tv.vocab_argmax_topk(t["logits"], k=0, want_lse=False, want_max=False,
+                                                                  ws=wsv, outputs=voc), 3),
+              ("accept_longest_path", lambda: tv.accept_longest_path(t["parent"], t["tok"], voc[0], t["node_off"],
+                                                                     max_nodes=Nr, max_depth=19, outputs=acc), 1)]
+
+        def step():
+            for _, f, _ in ks:
+                f()
+        return step, ks
+    sets = [dev_set(d, keys) for _ in range(copies_for(one))]
+    rows["step[blockpilot: 8 x 113 nodes (7 block sizes), prefix 8192, 32/8 heads bf16, V=151936]"] = _step_row(
+        torch, stream, sets, make4, n, one, pk,
+        "tv_tree_prep -> tree_verify_attn -> vocab_argmax_topk (argmax) -> accept_longest_path (path_acc: the "
+        "acceptance of all 7 block sizes); the block-size MLP runs once per request (its own row)")
+    del sets
+
+    # ---- workload 5: SpecOPD proposal tree (1024 nodes over a 4096-token trunk)
+    d = synth.specopd_tree()
+    n = d["parent"].size
+    keys = ("q", "k_pre", "v_pre", "k_tree", "v_tree", "lp", "lq", "parent", "node_off", "pre_off", "vis_prefix",
+            "branch_off", "mass_tok")
+    one = sum(np.asarray(d[k]).nbytes for k in keys)
+
+    def make5(t):
+        t["plen"] = to_dev(np.array([4096], np.int32), torch)
+        prep_o = (i32(n), i32(n), torch.empty((n, 16), dtype=torch.int64, device="cuda"), i32(n),
+                  torch.zeros(1, dtype=torch.int32, device="cuda"))
+        t["anc"] = prep_o[2]
+        attn = attn_call(t, n, n, 4096, 1, 32, 8, 128, 1, vis=t["vis_prefix"])
+        wsa = torch.empty(lib.tree_tv_alpha_workspace_size(n, V), dtype=torch.uint8, device="cuda")
+        ao = tuple(torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3))
+        ks = [("tv_tree_prep", lambda: tv.tv_tree_prep(t["parent"], t["node_off"], t["plen"], t["vis_prefix"], n, 16,
+                                                       outputs=prep_o), 1),
+              ("tree_verify_attn", attn, 2),
+              ("tree_tv_alpha", lambda: tv.tree_tv_alpha(t["lp"], t["lq"], t["branch_off"], t["mass_tok"], ws=wsa,
+                                                         outputs=ao), 1)]
+
+        def step():
+            for _, f, _ in ks:
+                f()
+        return step, ks
+    sets = [dev_set(d, keys) for _ in range(copies_for(one))]
+    rows["step[specopd: 1024 nodes (64 branches x 16), trunk 4096, 32/8 heads bf16, p,q V=151936]"] = _step_row(
+        torch, stream, sets, make5, n, one, pk,
+        "tv_tree_prep -> tree_verify_attn -> tree_tv_alpha (alpha, branch running product, softmax mass)")
+    del sets
+    return rows
+
+
+# ============================================================ host memory placement
+def _cpulist(text):
+    out = set()
+    for part in text.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            out.update(range(int(a), int(b) + 1))
+        elif part:
+            out.add(int(part))
+    return out
+
+
+def numa_report(torch, dev_index, buffers):
+    """Where the end-to-end inputs live: the GPU's NUMA node (sysfs), the
+    process's CPU affinity and the NUMA node of each CPU in it, and the nodes
+    holding the pages of the given pinned buffers (/proc/self/numa_maps)."""
+    rep = {}
+    try:
+        pr = torch.cuda.get_device_properties(dev_index)
+        bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            rep["gpu_pci"], rep["gpu_numa_node"] = bus, int(f.read())
+    except (OSError, AttributeError, ValueError, RuntimeError):
+        rep["gpu_numa_node"] = None
+    aff = sorted(os.sched_getaffinity(0))
+    rep["cpu_affinity"] = f"{len(aff)} cpus ({aff[0]}-{aff[-1]})" if aff else "none"
+    nodes = {}
+    try:
+        for nd in sorted(os.listdir("/sys/devices/system/node")):
+            if nd.startswith("node") and nd[4:].isdigit():
+                with open(f"/sys/devices/system/node/{nd}/cpulist") as f:
+                    cpus = _cpulist(f.read())
+                if cpus & set(aff):
+                    nodes[int(nd[4:])] = len(cpus & set(aff))
+    except OSError:
+        pass
+    rep["affinity_cpus_per_node"] = nodes
+    # page placement of each buffer: numa_maps gives per-mapping page counts
+    try:
+        spans = []
+        with open("/proc/self/maps") as f:
+            for line in f:
+                a, b = line.split()[0].split("-")
+                spans.append((int(a, 16), int(b, 16)))
+        counts = {}
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                parts = line.split()
+                counts[int(parts[0], 16)] = {p.split("=")[0]: int(p.split("=")[1]) for p in parts[1:]
+                                             if p.startswith("N") and "=" in p}
+        pages = {}
+        for t in buffers:
+            addr = t.data_ptr()
+            for a, b in spans:
+                if a <= addr < b:
+                    for k, v in counts.get(a, {}).items():
+                        pages[k] = pages.get(k, 0) + v
+                    break
+        rep["pinned_pages_per_node"] = pages
+    except OSError:
+        rep["pinned_pages_per_node"] = None
+    return rep
+
+
 def max_over_ranks(x, dist, device):
     """The largest of every rank's x (the job's time is its slowest rank's)."""
     if dist is None:
@@ -703,7 +963,9 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host
     e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), t_host * 1e3) / n_e2e, dist, "cuda")
+    placement = numa_report(torch, local, list(pinned.values()))
     e2e = {"value": whole_job_rate(K, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "placement": placement,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "inputs": "pinned host memory; small inputs copied per step (overlapping the previous step), "
                      "logits read in place (only the kept rows cross the host link)"}
@@ -711,6 +973,8 @@ def gpu_arm(args):
     rows = None
     if not args.no_rows and rank == 0:
         rows = measure_rows(tv, torch, pk, stream, only=args.rows_only)
+        if args.rows_only is None or re.search(args.rows_only, "step"):
+            rows.update(config_steps(tv, torch, pk, stream))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -722,7 +986,9 @@ def gpu_arm(args):
         line["rows"] = rows
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample, _ = run_cpu_oracle(d, args.rho, steps=64, warmup=2)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        v1, _, sample1, _ = run_cpu_oracle(d, args.rho, steps=8, warmup=1, cores=1)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                                "single_thread": {"value": v1, "unit": UNIT, "cores": 1, "sample": sample1}}
     if dist:
         dist.barrier()
         dist.destroy_process_group()

@@ -187,7 +187,7 @@ int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld
  * vocab_argmax_topk; the caller still provides the inputs and outputs.
  *   - Sizes whose scratch need (vocab_argmax_topk_workspace_size) exceeds
  *     TV_NOALLOC_SCRATCH_BYTES are rejected with TV_EWORKSPACE (for V = 151936:
- *     up to 1698 rows).
+ *     up to 24528 rows with k <= 8, 12985 with k <= 16).
  *   - The first call on a device looks up the array's device address (one
  *     runtime query, no allocation); make that first call before any stream
  *     capture on that device.

@@ -327,22 +327,29 @@ __global__ void __launch_bounds__(128) vocab_merge_kernel(
 // ---------------------------------------------------------------------------
 // Streaming variant (used whenever rows and chunk tails are 16-byte aligned).
 //
-// A persistent grid of CTAs walks the (row, chunk) items round-robin.  Each
-// CTA keeps a ring of 8192-element chunks in shared memory, filled by
-// cp.async.bulk copies that thread 0 issues a ring's length ahead, so loads
-// stay in flight while earlier chunks are reduced.  Per chunk: thread maxima
-// (bf16 pairs at a time), then each warp's top few thread maxima; the chunk
-// max is the largest of those and the top-k threshold tau their k-th largest,
-// so at least k distinct elements are >= tau and every member of the chunk's
-// top-k is.  Threads whose own maximum is below tau skip the candidate
-// scan; the others write their candidates straight into the chunk's partial
-// record.  Nothing is ranked per chunk: the per-row merge ranks all
-// candidates, so a chunk costs one block barrier and no serial section.
+// A persistent grid of CTAs walks the (row, chunk) items in claim order.  In
+// each CTA a producer warp claims items from a global counter (SMs that run
+// slower simply take fewer) and copies each 8192-element chunk into the next
+// slot of a shared-memory ring with a 1-D bulk copy, a ring's length ahead.
+// Compute warp w owns segment w of every chunk: its 1024 contiguous
+// elements.  Per segment it records only the maximum and, for the
+// log-sum-exp, the sum of exp(x - maximum); there is no block barrier and no
+// candidate list, so the warps never wait for one another.
+//
+// A merge kernel (one warp per row) follows.  Row max = the largest segment
+// maximum; log-sum-exp from the segment sums in (chunk, segment) order; the
+// top-k threshold tau = the k-th largest segment maximum: k distinct
+// elements (one per segment) are >= tau, so every member of the row's top-k
+// is >= tau and lies in a segment whose maximum reaches tau (about k of
+// them).  Only those segments are read again; their elements >= tau,
+// typically a dozen, are ranked exactly by (value desc, index asc).
 // ---------------------------------------------------------------------------
-// ring of 8192-element chunks: 3 x 16 KB for bf16 (four CTAs per SM: more chunks in
-// flight per SM beat deeper rings), 3 x 32 KB for fp32
+// ring of 8192-element chunks: 3 x 16 KB for bf16 (four CTAs per SM), 3 x 32 KB for fp32
 template <typename T> constexpr int stream_stages() { return 3; }
 template <typename T> constexpr int stream_chunk_bytes() { return kVChunk * static_cast<int>(sizeof(T)); }
+constexpr int kSegs = kVThreads / 32;        // segments per chunk = compute warps
+constexpr int kSegLen = kVChunk / kSegs;     // 1024 elements
+constexpr int kMaxFastSegs = 256;            // segment maxima a merge keeps in registers (8 per lane)
 
 __device__ __forceinline__ uint32_t sm_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -376,331 +383,19 @@ __device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   }
   return false;
 }
-
-// 32 values per thread; value t of thread tid is element (t/VEC*256 + tid)*VEC + t%VEC,
-// VEC = elements per 16-byte vector.  With TAIL, entries at or past n_valid
-// become -inf (only the last chunk of a row is partial).
-template <typename T, bool TAIL>
-__device__ __forceinline__ void stage_values(const uint8_t* st, int n_valid, float* v) {
-  constexpr int VEC = 16 / static_cast<int>(sizeof(T));
-#pragma unroll
-  for (int j = 0; j < kVPerThread / VEC; ++j) {
-    const int e0 = (j * kVThreads + threadIdx.x) * VEC;
-    const uint4 w = *reinterpret_cast<const uint4*>(st + e0 * sizeof(T));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    if constexpr (sizeof(T) == 2) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        v[8 * j + 2 * q] = bf16_lo(ws[q]);
-        v[8 * j + 2 * q + 1] = bf16_hi(ws[q]);
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[4 * j + q] = __uint_as_float(ws[q]);
-    }
-    if (TAIL) {
-#pragma unroll
-      for (int q = 0; q < VEC; ++q)
-        if (e0 + q >= n_valid) v[VEC * j + q] = -INFINITY;
-    }
-  }
-}
-
-// Partial of one streamed chunk: max, sum of exp(x - max), and every element
-// >= the chunk threshold (up to kSCand of them; ovf = 1 when there were more).
-// The threshold below leaves about 22 candidates per chunk on Gaussian
-// logits for k <= 8; more than 128 occurred in none of 2 * 10^5 simulated
-// chunks (more than 96: 3 * 10^-5 of them).
-constexpr int kSCand = 128;
-struct StreamPart {
-  float m, s;
-  int cnt, ovf;
-  int idx[kSCand];
-  float val[kSCand];
-};
-
 __device__ __forceinline__ bool bar_wait_fast(uint32_t bar, uint32_t parity) {
   return bar_try(bar, parity) || bar_wait(bar, parity);
-}
-
-// Warp-wide float maximum / minimum in one instruction (sm_100 family).
-__device__ __forceinline__ float redux_max(float v) {
-  float r;
-  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-__device__ __forceinline__ float redux_min(float v) {
-  float r;
-  asm("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-// k-th largest (k >= 1) of one value per lane: k - 1 rounds that drop the
-// first lane holding the current maximum.
-__device__ __forceinline__ float warp_kth_largest(float v, int k) {
-  for (int r = 1; r < k; ++r) {
-    const float m = redux_max(v);
-    const unsigned hit = __ballot_sync(0xffffffffu, v == m);
-    if (static_cast<int>(threadIdx.x & 31) == __ffs(hit) - 1) v = -INFINITY;
-  }
-  return redux_max(v);
-}
-
-// Chunk threshold: each of the 8 warps contributes its largest thread maximum
-// (k <= 8), or its two largest from distinct threads (k <= 16), and tau is
-// the smallest contribution.  At least 8 (16) distinct elements of the chunk
-// are >= tau, so every member of its top-k is.  One min-reduction, no ranking.
-template <int KMAX> constexpr int tau_per_warp() { return KMAX <= 8 ? 1 : 2; }
-
-__device__ __forceinline__ void bar_named(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ bool bar_named_and(int id, int n, bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\tbar.red.and.pred b, %2, %3, a;\n\tselp.u32 %0, 1, 0, b;\n\t}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
 }
 __device__ __forceinline__ void bar_arrive_plain(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Workspace header of the streaming path (zeroed before every launch).
-struct StreamHdr {
-  int status;   // nonzero: a wait ran out
-  int claim;    // next unclaimed (row, chunk) item
-};
-constexpr size_t kStreamHdrBytes = 256;
-
-// `status0` is 0 except when the caller's process plants a failure to test
-// the failure path (TV_TEST_VOCAB_STATUS, read on the host).
-__global__ void stream_hdr_clear_kernel(StreamHdr* hdr, int status0) {
-  griddep_wait();
-  griddep_release();
-  hdr->status = status0;
-  hdr->claim = 0;
+// Warp-wide float maximum in one instruction (sm_100 family).
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
-
-// CTA = 8 compute warps + 1 producer warp.  The producer's lane 0 claims
-// (row, chunk) items from a global counter, so SMs that run slower simply
-// take fewer items, and copies each into the next free ring slot; compute
-// warps never wait on its memory round trips.  Per item the compute warps
-// take thread maxima (bf16 pairs at a time), each warp's largest (k <= 8)
-// or two largest (k <= 16) thread maxima, one named barrier, then the chunk
-// max and the threshold tau (smallest contribution) and the candidates
-// >= tau, reread from the slot.  After the barrier of item i
-// thread 0 frees the slot of item i - 1 and closes that item's record (its
-// candidates are final there).
-constexpr int kStreamThreads = kVThreads + 32;
-
-template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(kStreamThreads, 4) vocab_stream_kernel(
-    const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows,
-    int n_chunks, StreamPart* __restrict__ part, StreamHdr* __restrict__ hdr) {
-  constexpr int EPT = kVPerThread;                        // 32 values per thread
-  constexpr int VEC = 16 / static_cast<int>(sizeof(T));   // elements per 16 B
-  constexpr int CH = kVChunk;                             // 8192 elements per chunk
-  constexpr int NW = kVThreads / 32;
-  constexpr int P = tau_per_warp<KMAX>();
-  constexpr int NV = NW * P;
-  static_assert(NV <= 32, "threshold values must fit one warp");
-  constexpr int S = stream_stages<T>();
-  constexpr int kSChunkBytes = stream_chunk_bytes<T>();
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[S], empty[S];
-  __shared__ int s_item[S], s_chunk[S];
-  __shared__ __align__(16) float s_top[2][NV];
-  __shared__ float s_wsum[2][NW];
-  __shared__ int s_cnt[2];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
-  griddep_wait();
-  griddep_release();
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&empty[s])) : "memory");
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    s_cnt[0] = s_cnt[1] = 0;
-  }
-  __syncthreads();
-
-  if (warp == NW) {   // ------------------------------------------------ producer
-    if (lane != 0) return;
-    // two claims in flight: the item for this slot and the next one
-    int a0 = atomicAdd(&hdr->claim, 1);
-    int a1 = a0 < items ? atomicAdd(&hdr->claim, 1) : items;
-    for (int q = 0;; ++q) {
-      const int s = q % S;
-      const int item = a0;
-      a0 = a1;
-      if (a1 < items) a1 = atomicAdd(&hdr->claim, 1);
-      if (q >= S && !bar_wait_fast(sm_u32(&empty[s]), ((q / S) - 1) & 1)) {
-        atomicExch(&hdr->status, 1);
-        return;
-      }
-      if (item >= items) {   // no more work: an empty slot tells the compute warps
-        s_item[s] = -1;
-        bar_arrive_plain(sm_u32(&full[s]));
-        return;
-      }
-      const int row = item / n_chunks, c = item - row * n_chunks;
-      const int src = row_idx ? row_idx[row] : row;
-      s_item[s] = item;
-      s_chunk[s] = c;
-      const int n = min(CH, V - c * CH);
-      bulk_g2s(sm_u32(ring + s * kSChunkBytes), logits + static_cast<int64_t>(src) * ld + static_cast<int64_t>(c) * CH,
-               static_cast<uint32_t>(n * sizeof(T)), sm_u32(&full[s]));
-    }
-  }
-
-  // ------------------------------------------------------------- compute warps
-  float rec_m = 0.f, rec_s = 0.f;   // thread 0: max and sum of the previous item
-  int prev = -1;
-  for (int it = 0;; ++it) {
-    const int s = it % S, b = it & 1;
-    const bool ok = bar_wait_fast(sm_u32(&full[s]), (it / S) & 1);
-    const int item = ok ? s_item[s] : -1;
-    const int c = ok ? s_chunk[s] : 0;
-    const int base = c * CH;
-    const int n_valid = item >= 0 ? min(CH, V - base) : 0;
-    const uint8_t* st = ring + s * kSChunkBytes;
-    float my_max;
-    float v[EPT];
-    __nv_bfloat162 pm[4];   // packed max of each of this thread's 16-byte vectors
-    if (sizeof(T) == 2 && !LSE && n_valid == CH) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
-        pm[j] = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x),
-                                *reinterpret_cast<const __nv_bfloat162*>(&w.y)),
-                        __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z),
-                                *reinterpret_cast<const __nv_bfloat162*>(&w.w)));
-      }
-      const __nv_bfloat162 m2 = __hmax2(__hmax2(pm[0], pm[1]), __hmax2(pm[2], pm[3]));
-      my_max = fmaxf(__low2float(m2), __high2float(m2));
-    } else {
-      if (n_valid == CH) stage_values<T, false>(st, CH, v);
-      else stage_values<T, true>(st, n_valid, v);
-      float m4[4] = {v[0], v[1], v[2], v[3]};
-#pragma unroll
-      for (int t = 4; t < EPT; ++t) m4[t & 3] = fmaxf(m4[t & 3], v[t]);
-      my_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    }
-    const float wmax = redux_max(my_max);
-    if (lane == 0) s_top[b][warp * P] = wmax;
-    if constexpr (P > 1) {
-      float mine = my_max, top = wmax;
-#pragma unroll
-      for (int p = 1; p < P; ++p) {
-        const unsigned hit = __ballot_sync(0xffffffffu, mine == top);
-        if (lane == __ffs(hit) - 1) mine = -INFINITY;
-        top = redux_max(mine);
-        if (lane == 0) s_top[b][warp * P + p] = top;
-      }
-    }
-    if constexpr (LSE) {   // sum of exp(x - warp max)
-      float sum = 0.f;
-      if (wmax != -INFINITY) {
-        const float mb = wmax * kLog2e;
-#pragma unroll
-        for (int t = 0; t < EPT; ++t) sum += ex2(fmaf(v[t], kLog2e, -mb));
-      }
-      sum = warp_sum(sum);
-      if (lane == 0) s_wsum[b][warp] = sum;
-    }
-    const bool all_ok = bar_named_and(1, kVThreads, ok);   // block-uniform
-    if (!all_ok) {
-      if (tid == 0) atomicExch(&hdr->status, 1);
-      return;
-    }
-    if (tid == 0) {
-      // the previous item's slot was last read (candidate pass) before this barrier
-      if (it > 0) bar_arrive_plain(sm_u32(&empty[(it - 1) % S]));
-      if (prev >= 0) {                        // candidates of the previous item are final
-        StreamPart* o = part + prev;
-        const int cnt = s_cnt[b ^ 1];
-        s_cnt[b ^ 1] = 0;
-        o->m = rec_m;
-        o->s = rec_s;
-        o->cnt = min(cnt, kSCand);
-        o->ovf = cnt > kSCand;
-      }
-    }
-    if (item < 0) return;
-    const float tv = lane < NV ? s_top[b][lane] : -INFINITY;
-    const float M = redux_max(tv);
-    const float tau = KMAX == 1 ? M : redux_min(lane < NV ? tv : INFINITY);
-    if (tid == 0) {
-      float ssum = 0.f;
-      if constexpr (LSE) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float wm = s_top[b][w * P];
-          if (wm != -INFINITY) ssum += s_wsum[b][w] * ex2((wm - M) * kLog2e);
-        }
-      }
-      rec_m = M;
-      rec_s = ssum;
-    }
-    prev = item;
-    if (my_max >= tau) {
-      StreamPart* out = part + item;
-      auto put = [&](float val, int e) {
-        const int pos = atomicAdd(&s_cnt[b], 1);
-        if (pos < kSCand) {
-          out->val[pos] = val;
-          out->idx[pos] = base + e;
-        }
-      };
-      if (sizeof(T) == 2 && !LSE && n_valid == CH) {
-        // reread only the vectors whose maximum reaches tau (the slot is freed
-        // at the next barrier); tau is one of the chunk's elements, so exact
-        // in bf16
-        const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (!__hge2_mask(pm[j], t2)) continue;
-          const uint4 w = *reinterpret_cast<const uint4*>(st + (j * kVThreads + tid) * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const unsigned msk = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q]), t2);
-            if (msk) {
-              const int e = (j * kVThreads + tid) * VEC + 2 * q;
-              if (msk & 0xffffu) put(bf16_lo(ws[q]), e);
-              if (msk >> 16) put(bf16_hi(ws[q]), e + 1);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int t = 0; t < EPT; ++t)
-          if (v[t] >= tau) put(v[t], ((t / VEC) * kVThreads + tid) * VEC + (t % VEC));
-      }
-    }
-  }
-}
-
-// One warp per row.  In one round trip the warp reads every chunk header
-// (max, sum, candidate count, overflow; one 16-byte load per lane) and the
-// first 32 entries of every chunk's candidate list, and takes the row max
-// and sum.  Row threshold: the KMAX-th largest chunk maximum; KMAX
-// distinct elements reach it, so every member of the row's top-k is >= it,
-// and only chunks whose maximum reaches it (about KMAX of them) are opened.
-// Their candidates >= the threshold (a chunk that overflowed is rescanned
-// from the logits) are compacted into a shared buffer, usually a dozen
-// entries, which a 32-lane bitonic sort orders.  Rows with more than 32
-// buffered candidates use per-lane lists; rows with more than the buffer
-// holds (heavy ties) or more than 32 chunks take the plain path over every
-// record.
-constexpr int kMergeWarps = 4;
-constexpr int kMergeBuf = 128;
 
 // Sort one (value, index) pair per lane by (value desc, index asc): lane 0 best.
 __device__ __forceinline__ void warp_bitonic_desc(float& v, int& i) {
@@ -719,182 +414,215 @@ __device__ __forceinline__ void warp_bitonic_desc(float& v, int& i) {
   }
 }
 
-template <typename T, int KMAX, bool LSE>
-__global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel(
-    const StreamPart* __restrict__ part, int n_chunks, int rows, const T* __restrict__ logits, int V,
-    int64_t ld, const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax,
-    int32_t* __restrict__ topk_idx, float* __restrict__ topk_val, float* __restrict__ row_max,
-    float* __restrict__ row_lse, const StreamHdr* __restrict__ hdr) {
-  __shared__ float s_bv[kMergeWarps][kMergeBuf];
-  __shared__ int s_bi[kMergeWarps][kMergeBuf];
+// Record of one (row, chunk) item: per segment its maximum (-inf when empty)
+// and sum of exp(x - maximum) (log-sum-exp calls only).
+struct StreamRec {
+  float m[kSegs];
+  float s[kSegs];
+};
+
+// Workspace header of the streaming path (reset before every call).
+struct StreamHdr {
+  int status;   // nonzero: a wait ran out
+  int claim;    // next unclaimed (row, chunk) item
+};
+constexpr size_t kStreamHdrBytes = 256;
+
+// `status0` is 0 except when the caller's process plants a failure to test
+// the failure path (TV_TEST_VOCAB_STATUS, read on the host).
+__global__ void stream_hdr_clear_kernel(StreamHdr* hdr, int status0) {
   griddep_wait();
   griddep_release();
-  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const int row = blockIdx.x * kMergeWarps + wl;
-  if (row >= rows) return;
-  const int src = row_idx ? row_idx[row] : row;
-  const int dst = src;
-  if (__ldcg(&hdr->status) != 0) {
-    // a bounded wait of the streaming kernel ran out: its chunk records are
-    // incomplete, so every row reports failure instead of a stale merge
-    if (lane == 0) {
-      argmax[dst] = -1;
-      if (row_max) row_max[dst] = __int_as_float(0x7fc00000);
-      if (LSE && row_lse) row_lse[dst] = __int_as_float(0x7fc00000);
-    }
-    if (k > 0 && lane < k) {
-      if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = -1;
-      if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = __int_as_float(0x7fc00000);
-    }
-    return;
-  }
-  const StreamPart* gp = part + static_cast<int64_t>(row) * n_chunks;
-  const T* x = logits + static_cast<int64_t>(src) * ld;
-  auto logit = [&](int e) -> float {
-    if constexpr (sizeof(T) == 2) return bf16_at(reinterpret_cast<const uint16_t*>(x) + e);
-    else return reinterpret_cast<const float*>(x)[e];
-  };
-  auto emit_head = [&](int arg, float M, float S) {
-    argmax[dst] = arg;
-    if (row_max) row_max[dst] = M;
-    if (LSE && row_lse) row_lse[dst] = M + logf(S);
-  };
+  hdr->status = status0;
+  hdr->claim = 0;
+}
 
-  if (n_chunks <= 32) {
-    // one round trip: every chunk's header (lane c) and the first 32 entries
-    // of every chunk's candidate list (lane l: entry l of each) at once
-    float mc = -INFINITY, sc = 0.f;
-    int cc = 0, oc = 0;
-    if (lane < n_chunks) {
-      const uint4 h = __ldcg(reinterpret_cast<const uint4*>(gp + lane));
-      mc = __uint_as_float(h.x); sc = __uint_as_float(h.y);
-      cc = static_cast<int>(h.z); oc = static_cast<int>(h.w);
-    }
-    float cv[32];
-    int ci[32];
+// Elements of segment `seg` of a row visible to this lane: 4 (bf16) or 8
+// (fp32) 16-byte vectors, lane-interleaved; entries at or past V become -inf.
+template <typename T>
+__device__ __forceinline__ void seg_values(const uint8_t* p, int e_first, int V, float* v) {
+  constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+  constexpr int NV = kSegLen / VEC / 32;   // vectors per lane
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      cv[c] = -INFINITY;
-      ci[c] = INT32_MAX;
-      if (c < n_chunks) { cv[c] = __ldcg(&gp[c].val[lane]); ci[c] = __ldcg(&gp[c].idx[lane]); }
-    }
-    const float M = redux_max(mc);
-    float S = 0.f;
-    if (LSE) S = warp_sum(mc != -INFINITY ? sc * ex2((mc - M) * kLog2e) : 0.f);
-    // rank of each chunk maximum (value desc, chunk asc); tau = rank KMAX - 1
-    float tau = M;
-    if (KMAX > 1) {
-      int rank = 0;
+  for (int j = 0; j < NV; ++j) {
+    const int e0 = e_first + (j * 32 + lane) * VEC;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (e0 < V) w = *reinterpret_cast<const uint4*>(p + static_cast<size_t>((j * 32 + lane) * VEC) * sizeof(T));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (sizeof(T) == 2) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float o = __shfl_sync(0xffffffffu, mc, c);
-        rank += c < n_chunks && (o > mc || (o == mc && c < lane));
+      for (int q = 0; q < 4; ++q) {
+        v[8 * j + 2 * q] = e0 < V ? bf16_lo(ws[q]) : -INFINITY;
+        v[8 * j + 2 * q + 1] = e0 < V ? bf16_hi(ws[q]) : -INFINITY;
       }
-      const unsigned sel = __ballot_sync(0xffffffffu, lane < n_chunks && rank == KMAX - 1);
-      tau = sel ? __shfl_sync(0xffffffffu, mc, __ffs(sel) - 1) : -INFINITY;   // fewer chunks than KMAX
-    }
-    const unsigned surv = __ballot_sync(0xffffffffu, lane < n_chunks && mc >= tau);
-    const unsigned ovfm = __ballot_sync(0xffffffffu, oc != 0);
-    int nb = 0;   // buffered candidates, warp-uniform
-    auto append = [&](bool keep, float v, int e) {
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      const int pos = nb + __popc(bal & ((1u << lane) - 1u));
-      if (keep && pos < kMergeBuf) { s_bv[wl][pos] = v; s_bi[wl][pos] = e; }
-      nb += __popc(bal);
-    };
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      if (!((surv & ~ovfm) >> c & 1u)) continue;
-      const int n = __shfl_sync(0xffffffffu, cc, c);
-      append(lane < n && cv[c] >= tau, cv[c], ci[c]);
-    }
-    // rare: opened lists longer than one warp's worth
-    for (unsigned todo = surv & ~ovfm; todo; todo &= todo - 1u) {
-      const int c = __ffs(todo) - 1;
-      const int n = __shfl_sync(0xffffffffu, cc, c);
-      for (int q0 = 32; q0 < n; q0 += 32) {
-        const int q = q0 + lane;
-        const bool in = q < n;
-        const float x = in ? __ldcg(&gp[c].val[q]) : -INFINITY;
-        const int e = in ? __ldcg(&gp[c].idx[q]) : INT32_MAX;
-        append(in && x >= tau, x, e);
-      }
-    }
-    // opened chunks whose candidate list overflowed: rescan their logits
-    unsigned rescan = surv & ovfm;
-    while (rescan && nb <= kMergeBuf) {
-      const int c = __ffs(rescan) - 1;
-      rescan &= rescan - 1u;
-      const int e1 = min(V, (c + 1) * kVChunk);
-      for (int e0 = c * kVChunk; e0 < e1 && nb <= kMergeBuf; e0 += 32) {
-        const int e = e0 + lane;
-        const float xv = e < e1 ? logit(e) : -INFINITY;
-        append(e < e1 && xv >= tau, xv, e);
-      }
-    }
-    __syncwarp();
-    if (nb <= 32) {
-      float v = lane < nb ? s_bv[wl][lane] : -INFINITY;
-      int i = lane < nb ? s_bi[wl][lane] : INT32_MAX;
-      warp_bitonic_desc(v, i);
-      const int arg = __shfl_sync(0xffffffffu, i, 0);
-      if (lane == 0) emit_head(arg, M, S);
-      if (k > 0 && lane < k) {
-        if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = i;
-        if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = v;
-      }
-      return;
-    }
-    if (nb <= kMergeBuf) {
-      float lv[KMAX];
-      int li[KMAX];
-#pragma unroll
-      for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
-      for (int t = lane; t < nb; t += 32) list_insert<KMAX>(lv, li, s_bv[wl][t], s_bi[wl][t]);
-      float ov[KMAX];
-      int oi[KMAX];
-      warp_merge_lists<KMAX>(lv, li, ov, oi);
-      if (lane == 0) emit_head(oi[0], M, S);
-      if (k > 0 && lane < k) {
-        float val = ov[0];
-        int idx = oi[0];
-#pragma unroll
-        for (int q = 1; q < KMAX; ++q)
-          if (lane == q) { val = ov[q]; idx = oi[q]; }
-        if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = idx;
-        if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = val;
-      }
-      return;
-    }
-  }
-
-  // plain path: every record, every overflowed chunk rescanned in full
-  float M = -INFINITY;
-  for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, gp[c].m);
-  M = warp_max(M);
-  float S = 0.f;
-  if (LSE) {
-    for (int c = lane; c < n_chunks; c += 32)
-      if (gp[c].m != -INFINITY) S += gp[c].s * ex2((gp[c].m - M) * kLog2e);
-    S = warp_sum(S);
-  }
-  float lv[KMAX];
-  int li[KMAX];
-#pragma unroll
-  for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
-  for (int c = 0; c < n_chunks; ++c) {
-    if (!gp[c].ovf) {
-      const int n = gp[c].cnt;
-      for (int q = lane; q < n; q += 32) list_insert<KMAX>(lv, li, gp[c].val[q], gp[c].idx[q]);
     } else {
-      const int e1 = min(V, (c + 1) * kVChunk);
-      for (int e = c * kVChunk + lane; e < e1; e += 32) list_insert<KMAX>(lv, li, logit(e), e);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[4 * j + q] = e0 < V ? __uint_as_float(ws[q]) : -INFINITY;
     }
   }
+}
+// element number of value t of this lane within its segment
+template <typename T>
+__device__ __forceinline__ int seg_elem(int t) {
+  constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+  return ((t / VEC) * 32 + static_cast<int>(threadIdx.x & 31)) * VEC + t % VEC;
+}
+
+constexpr int kMergeBuf = 64;   // candidates a row's merge ranks in shared memory
+constexpr int kMergeWarps = 4;  // rows per merge CTA (one warp each)
+
+// Merge of one row by one warp: row max and log-sum-exp from the segment
+// records; tau = the KMAX-th largest segment maximum; the segments whose
+// maximum reaches tau are read again (two at a time, so that their loads
+// overlap) and their elements >= tau ranked.
+template <typename T, int KMAX, bool LSE>
+__device__ __noinline__ void merge_row(const StreamRec* __restrict__ rec, int n_chunks, const T* __restrict__ x,
+                                       int V, int dst, int k, int32_t* __restrict__ argmax,
+                                       int32_t* __restrict__ topk_idx, float* __restrict__ topk_val,
+                                       float* __restrict__ row_max, float* __restrict__ row_lse, float* s_bv,
+                                       int* s_bi) {
+  constexpr int SPL = kMaxFastSegs / 32;   // segment maxima per lane
+  constexpr int EPS = kSegLen / 32;        // elements per lane per segment
+  const int lane = threadIdx.x & 31;
+  const int nseg = n_chunks * kSegs;
+  const bool fast = nseg <= kMaxFastSegs;
+  auto seg_first = [&](int g) { return (g / kSegs) * kVChunk + (g % kSegs) * kSegLen; };
+  auto load_seg = [&](int g, float* v) {
+    seg_values<T>(reinterpret_cast<const uint8_t*>(x + seg_first(g)), seg_first(g), V, v);
+  };
+  float M = -INFINITY, S = 0.f, tau = -INFINITY;
+  // segment q * 32 + lane of the row in slot q
+  float sm[SPL];
+  if (fast) {
+    float ss[SPL];
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) {
+      const int g = q * 32 + lane;
+      sm[q] = g < nseg ? __ldcg(&rec[g / kSegs].m[g % kSegs]) : -INFINITY;
+      ss[q] = (LSE && g < nseg) ? __ldcg(&rec[g / kSegs].s[g % kSegs]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) M = fmaxf(M, sm[q]);
+    M = redux_max(M);
+    if constexpr (LSE) {
+#pragma unroll
+      for (int q = 0; q < SPL; ++q)
+        if (sm[q] != -INFINITY) S += ss[q] * ex2((sm[q] - M) * kLog2e);
+      S = warp_sum(S);
+    }
+    // tau: the KMAX-th largest segment maximum (-inf with fewer finite segments)
+    float w[SPL];
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) w[q] = sm[q];
+    for (int t = 0; t < KMAX; ++t) {
+      float mine = w[0];
+#pragma unroll
+      for (int q = 1; q < SPL; ++q) mine = fmaxf(mine, w[q]);
+      const float b = redux_max(mine);
+      tau = b;
+      const unsigned hit = __ballot_sync(0xffffffffu, mine == b);
+      if (lane == __ffs(hit) - 1) {   // drop one instance of b from this lane
+        bool done = false;
+#pragma unroll
+        for (int q = 0; q < SPL; ++q)
+          if (!done && w[q] == b) { w[q] = -INFINITY; done = true; }
+      }
+    }
+  } else {
+    for (int g = lane; g < nseg; g += 32) M = fmaxf(M, __ldcg(&rec[g / kSegs].m[g % kSegs]));
+    M = redux_max(M);
+    if constexpr (LSE) {
+      for (int g = lane; g < nseg; g += 32) {
+        const float m = __ldcg(&rec[g / kSegs].m[g % kSegs]);
+        if (m != -INFINITY) S += __ldcg(&rec[g / kSegs].s[g % kSegs]) * ex2((m - M) * kLog2e);
+      }
+      S = warp_sum(S);
+    }
+  }
+  // candidates >= tau of the segments whose maximum reaches tau
+  int nb = 0;
+  bool overflow = !fast;   // too many segments to select among: rank every element
+  auto append = [&](const float* v, int g) {
+#pragma unroll
+    for (int t = 0; t < EPS; ++t) {
+      const bool keep = v[t] >= tau && v[t] != -INFINITY;
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (bal) {
+        const int pos = nb + __popc(bal & ((1u << lane) - 1u));
+        if (keep && pos < kMergeBuf) { s_bv[pos] = v[t]; s_bi[pos] = seg_first(g) + seg_elem<T>(t); }
+        nb += __popc(bal);
+      }
+    }
+  };
+  if (fast) {
+    int pend = -1;   // a selected segment waiting for a partner
+#pragma unroll 1
+    for (int q = 0; q < SPL && !overflow; ++q) {
+      unsigned sel = __ballot_sync(0xffffffffu, sm[q] != -INFINITY && sm[q] >= tau);
+      while (sel && !overflow) {
+        const int g = q * 32 + __ffs(sel) - 1;
+        sel &= sel - 1u;
+        if (pend < 0) {
+          pend = g;
+          continue;
+        }
+        float v0[EPS], v1[EPS];
+        load_seg(pend, v0);
+        load_seg(g, v1);
+        append(v0, pend);
+        append(v1, g);
+        pend = -1;
+        overflow = nb > kMergeBuf;
+      }
+    }
+    if (pend >= 0 && !overflow) {
+      float v0[EPS];
+      load_seg(pend, v0);
+      append(v0, pend);
+      overflow = nb > kMergeBuf;
+    }
+  }
+  __syncwarp();
   float ov[KMAX];
   int oi[KMAX];
-  warp_merge_lists<KMAX>(lv, li, ov, oi);
-  if (lane == 0) emit_head(oi[0], M, S);
+  if (!overflow && nb <= 32) {
+    float v = lane < nb ? s_bv[lane] : -INFINITY;
+    int i = lane < nb ? s_bi[lane] : INT32_MAX;
+    warp_bitonic_desc(v, i);
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) {
+      ov[q] = __shfl_sync(0xffffffffu, v, q);
+      oi[q] = __shfl_sync(0xffffffffu, i, q);
+    }
+  } else {
+    // per-lane sorted lists, then KMAX rounds of warp merging: over the
+    // buffer, or (heavy ties) over every element of every segment that can
+    // hold a candidate
+    float lv[KMAX];
+    int li[KMAX];
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) { lv[q] = -INFINITY; li[q] = INT32_MAX; }
+    if (!overflow) {
+      for (int t = lane; t < nb; t += 32) list_insert<KMAX>(lv, li, s_bv[t], s_bi[t]);
+    } else {
+      for (int g = 0; g < nseg; ++g) {
+        const float m = __ldcg(&rec[g / kSegs].m[g % kSegs]);
+        if (m == -INFINITY || m < tau) continue;
+        float v[EPS];
+        load_seg(g, v);
+#pragma unroll
+        for (int t = 0; t < EPS; ++t)
+          if (v[t] != -INFINITY) list_insert<KMAX>(lv, li, v[t], seg_first(g) + seg_elem<T>(t));
+      }
+    }
+    warp_merge_lists<KMAX>(lv, li, ov, oi);
+  }
+  if (lane == 0) {
+    argmax[dst] = oi[0];
+    if (row_max) row_max[dst] = M;
+    if (LSE && row_lse) row_lse[dst] = M + logf(S);
+  }
   if (k > 0 && lane < k) {
     float val = ov[0];
     int idx = oi[0];
@@ -906,6 +634,140 @@ __global__ void __launch_bounds__(32 * kMergeWarps, 1) vocab_stream_merge_kernel
   }
 }
 
+// Failure outputs of one row (a bounded wait ran out somewhere in the grid).
+__device__ __forceinline__ void fail_row(int dst, int k, int32_t* argmax, int32_t* topk_idx, float* topk_val,
+                                         float* row_max, float* row_lse, int lane) {
+  const float nan = __int_as_float(0x7fc00000);
+  if (lane == 0) {
+    argmax[dst] = -1;
+    if (row_max) row_max[dst] = nan;
+    if (row_lse) row_lse[dst] = nan;
+  }
+  if (lane < k) {
+    if (topk_idx) topk_idx[static_cast<int64_t>(dst) * k + lane] = -1;
+    if (topk_val) topk_val[static_cast<int64_t>(dst) * k + lane] = nan;
+  }
+}
+
+constexpr int kStreamThreads = kVThreads + 32;   // 8 compute warps + 1 producer warp
+
+template <typename T, bool LSE>
+__global__ void __launch_bounds__(kStreamThreads, 4) vocab_stream_kernel(
+    const T* __restrict__ logits, int V, int64_t ld, const int32_t* __restrict__ row_idx, int rows, int n_chunks,
+    StreamRec* __restrict__ rec, StreamHdr* __restrict__ hdr) {
+  constexpr int EPT = kSegLen / 32;                        // values per lane per chunk
+  constexpr int NW = kSegs;
+  constexpr int S = stream_stages<T>();
+  constexpr int kSChunkBytes = stream_chunk_bytes<T>();
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[S], empty[S];
+  __shared__ int s_item[S], s_chunk[S];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int items = rows * n_chunks;          // < 2^31: rows <= 65535, chunks <= 2^15
+  griddep_wait();
+  griddep_release();
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(&full[s])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sm_u32(&empty[s])), "r"(NW) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == NW) {   // ------------------------------------------------ producer
+    if (lane != 0) return;
+    // two claims in flight: the item for this slot and the next one
+    int a0 = atomicAdd(&hdr->claim, 1);
+    int a1 = a0 < items ? atomicAdd(&hdr->claim, 1) : items;
+    for (int q = 0;; ++q) {
+      const int s = q % S;
+      const int item = a0;
+      a0 = a1;
+      if (a1 < items) a1 = atomicAdd(&hdr->claim, 1);
+      if (q >= S && !bar_wait_fast(sm_u32(&empty[s]), ((q / S) - 1) & 1)) {
+        atomicExch(&hdr->status, 1);
+        return;   // compute warps waiting on this slot time out in turn
+      }
+      if (item >= items) {   // no more work: an empty slot tells the compute warps
+        s_item[s] = -1;
+        bar_arrive_plain(sm_u32(&full[s]));
+        return;
+      }
+      const int row = item / n_chunks, c = item - row * n_chunks;
+      const int src = row_idx ? row_idx[row] : row;
+      s_item[s] = item;
+      s_chunk[s] = c;
+      const int n = min(kVChunk, V - c * kVChunk);
+      bulk_g2s(sm_u32(ring + s * kSChunkBytes),
+               logits + static_cast<int64_t>(src) * ld + static_cast<int64_t>(c) * kVChunk,
+               static_cast<uint32_t>(n * sizeof(T)), sm_u32(&full[s]));
+    }
+  }
+
+  // ------------------------------------------------------------- compute warps
+  for (int it = 0;; ++it) {
+    const int s = it % S;
+    if (!bar_wait_fast(sm_u32(&full[s]), (it / S) & 1)) {
+      if (lane == 0) atomicExch(&hdr->status, 1);
+      return;
+    }
+    const int item = s_item[s];
+    if (item < 0) return;
+    const int c = s_chunk[s];
+    const int e_first = c * kVChunk + warp * kSegLen;
+    float v[EPT];
+    seg_values<T>(ring + s * kSChunkBytes + static_cast<size_t>(warp) * kSegLen * sizeof(T), e_first, V, v);
+    __syncwarp();
+    if (lane == 0) bar_arrive_plain(sm_u32(&empty[s]));   // this warp is done with the slot
+    float m4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+    for (int t = 4; t < EPT; ++t) m4[t & 3] = fmaxf(m4[t & 3], v[t]);
+    const float wmax = redux_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+    float wsum = 0.f;
+    if constexpr (LSE) {
+      if (wmax != -INFINITY) {
+        const float mb = wmax * kLog2e;
+#pragma unroll
+        for (int t = 0; t < EPT; ++t) wsum += ex2(fmaf(v[t], kLog2e, -mb));
+      }
+      wsum = warp_sum(wsum);
+    }
+    if (lane == 0) {
+      StreamRec* r = rec + item;
+      r->m[warp] = wmax;
+      r->s[warp] = wsum;
+    }
+  }
+}
+
+// One warp per row, after the stream: merge the row from its segment
+// records, or, if a wait of the stream ran out, report failure on the row.
+template <typename T, int KMAX, bool LSE>
+__global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
+    const StreamRec* __restrict__ rec, int n_chunks, int rows, const T* __restrict__ logits, int V, int64_t ld,
+    const int32_t* __restrict__ row_idx, int k, int32_t* __restrict__ argmax, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_val, float* __restrict__ row_max, float* __restrict__ row_lse,
+    const StreamHdr* __restrict__ hdr) {
+  __shared__ float s_bv[kMergeWarps][kMergeBuf];
+  __shared__ int s_bi[kMergeWarps][kMergeBuf];
+  griddep_wait();
+  griddep_release();
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int row = blockIdx.x * kMergeWarps + wl;
+  if (row >= rows) return;
+  const int src = row_idx ? row_idx[row] : row;
+  if (__ldcg(&hdr->status) != 0) {
+    // a bounded wait of the streaming kernel ran out: its records are
+    // incomplete, so every row reports failure instead of a stale merge
+    fail_row(src, k, argmax, topk_idx, topk_val, row_max, LSE ? row_lse : nullptr, lane);
+    return;
+  }
+  merge_row<T, KMAX, LSE>(rec + static_cast<int64_t>(row) * n_chunks, n_chunks,
+                          logits + static_cast<int64_t>(src) * ld, V, src, k, argmax, topk_idx, topk_val, row_max,
+                          row_lse, s_bv[wl], s_bi[wl]);
+}
 
 int sm_count_cached() {
   static const int n = [] {
@@ -938,25 +800,27 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
   const bool stream_ok = vec_ok && (static_cast<int64_t>(V) * sizeof(T)) % 16 == 0;
   if (stream_ok) {
     constexpr int smem = stream_stages<T>() * stream_chunk_bytes<T>();
-    if (!smem_limit(vocab_stream_kernel<T, KMAX, LSE>, smem)) return TV_ECUDA;
+    if (!smem_limit(vocab_stream_kernel<T, LSE>, smem)) return TV_ECUDA;
     const int items = rows * n_chunks;
     // Rows in page-locked host memory arrive over the host link, far slower
     // than HBM: a quarter of the SMs keep it busy and leave the rest to
     // kernels running beside this one.
-    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4) : 4 * sm_count_cached());
+    const int per_sm = sizeof(T) == 2 ? 4 : 2;   // shared memory: 3-slot rings of 16 KB / 32 KB chunks
+    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4)
+                                                           : per_sm * sm_count_cached());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
-    auto* sp = reinterpret_cast<StreamPart*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
+    auto* rec = reinterpret_cast<StreamRec*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
     static const int planted = [] {
       const char* e = std::getenv("TV_TEST_VOCAB_STATUS");
       return e ? std::atoi(e) : 0;
     }();
     int rc = launch_pdl(stream_hdr_clear_kernel, dim3(1), dim3(1), 0, st, hdr, planted);
     if (rc == TV_OK)
-      rc = launch_pdl(vocab_stream_kernel<T, KMAX, LSE>, dim3(grid), dim3(kStreamThreads), smem, st, logits, V, ld,
-                      row_idx, rows, n_chunks, sp, hdr);
+      rc = launch_pdl(vocab_stream_kernel<T, LSE>, dim3(grid), dim3(kStreamThreads), smem, st, logits, V, ld,
+                      row_idx, rows, n_chunks, rec, hdr);
     if (rc == TV_OK)
       rc = launch_pdl(vocab_stream_merge_kernel<T, KMAX, LSE>, dim3((rows + kMergeWarps - 1) / kMergeWarps),
-                      dim3(32 * kMergeWarps), 0, st, sp, n_chunks, rows, logits, V, ld, row_idx, k, argmax,
+                      dim3(32 * kMergeWarps), 0, st, rec, n_chunks, rows, logits, V, ld, row_idx, k, argmax,
                       topk_idx, topk_val, row_max, row_lse, hdr);
     return rc;
   }
@@ -990,8 +854,12 @@ TV_API size_t vocab_argmax_topk_workspace_size(int rows, int V, int k) {
   if (rows <= 0 || V <= 0) return 0;
   const size_t n_chunks = (static_cast<size_t>(V) + tv::kVChunk - 1) / tv::kVChunk;
   const size_t kmax = k <= 1 ? 1 : (k <= 8 ? 8 : 16);
-  const size_t part = std::max(2 * sizeof(float) + kmax * (sizeof(float) + sizeof(int)), sizeof(tv::StreamPart));
-  return tv::kStreamHdrBytes + static_cast<size_t>(rows) * n_chunks * part;
+  // the larger of the two paths' needs: fallback chunk partials, or the
+  // streaming header, row counters and per-chunk segment records
+  const size_t part = 2 * sizeof(float) + kmax * (sizeof(float) + sizeof(int));
+  const size_t fallback = static_cast<size_t>(rows) * n_chunks * part;
+  const size_t stream = tv::kStreamHdrBytes + static_cast<size_t>(rows) * n_chunks * sizeof(tv::StreamRec);
+  return std::max(fallback, stream);
 }
 
 TV_API int vocab_argmax_topk(const void* logits, int dtype, int rows, int V, int64_t ld,

@@ -676,3 +676,4 @@ def test_vocab_status_word_clear_after_a_normal_call(tv):
     sync()
     assert int(ws[:4].view(torch.int32).item()) == 0
     assert np.array_equal(host(am), ovoc.argmax_topk(x, 1)[0])
+

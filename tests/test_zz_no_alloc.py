@@ -82,15 +82,21 @@ def test_noalloc_row_gather(tv):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(tv):
-    # the first row count whose scratch need exceeds the fixed array; the
-    # buffers are real and sized for the call, and the entry point must
-    # refuse it on the host (TV_EWORKSPACE) before any launch
+    # the first row count whose scratch need exceeds the fixed array (k = 16,
+    # the largest per-row need); the buffers are real and sized for the call
+    # (about 4 GB of logits), and the entry point must refuse it on the host
+    # (TV_EWORKSPACE) before any launch
     lib = tv.load_library()
-    V, k = synth.QWEN3_VOCAB, 8
-    rows = 1
-    while lib.vocab_argmax_topk_workspace_size(rows, V, k) <= (32 << 20):
-        rows += 1
-    assert rows == 1699
+    V, k = synth.QWEN3_VOCAB, 16
+    lo, hi = 1, 65535
+    while lo < hi:                                        # largest accepted row count
+        mid = (lo + hi + 1) // 2
+        if lib.vocab_argmax_topk_workspace_size(mid, V, k) <= (32 << 20):
+            lo = mid
+        else:
+            hi = mid - 1
+    rows = lo + 1
+    assert lib.vocab_argmax_topk_workspace_size(rows, V, k) > (32 << 20)
     L = torch.zeros((rows, V), dtype=torch.bfloat16, device="cuda")
     am, ti, tvl, rm, rl = outputs(rows, k)
     with pytest.raises(tv.TVError) as e:
@@ -98,3 +104,4 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(tv):
     assert e.value.status == -4
     torch.cuda.synchronize()
     assert bool((am == -1).all())                         # nothing was written
+    del L
