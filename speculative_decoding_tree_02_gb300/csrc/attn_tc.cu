@@ -94,6 +94,66 @@ struct TcParams {
   int* err;
 };
 
+// Merge of the pieces of one (request, KV head, tile), by the CTA of its last
+// piece to finish: all threads, two per query row (64 columns each), pieces
+// in order, so the result does not depend on which piece finished last.
+template <int LIVE>
+__device__ __forceinline__ void merge_pieces(const AttnParams& p, int r, int n0, int node_first, int cnt, int g,
+                                             int kvh, int n_pieces, int nthreads) {
+  constexpr int kMaxP = 8;   // weights held in registers; more pieces recompute them
+  for (int rr = threadIdx.x >> 1; rr < LIVE; rr += nthreads / 2) {
+    const int mln = node_first + rr / g;
+    if (mln >= cnt) continue;
+    const int mhead = kvh * g + rr % g;
+    const int half = threadIdx.x & 1;
+    auto mslot = [&](int pc) {
+      return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + mln) * p.Hq +
+             mhead;
+    };
+    float2 ml[kMaxP];
+#pragma unroll
+    for (int i = 0; i < kMaxP; ++i) ml[i] = i < n_pieces ? __ldcg(&p.ws_ml[mslot(i)]) : make_float2(-INFINITY, 0.f);
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxP; ++i) M = fmaxf(M, ml[i].x);
+    for (int i = kMaxP; i < n_pieces; ++i) M = fmaxf(M, __ldcg(&p.ws_ml[mslot(i)].x));
+    float W = 0.f;
+    float acc[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+    auto add_piece = [&](float2 mi, int i) {
+      const float w = mi.y > 0.f ? ex2(mi.x - M) * mi.y : 0.f;   // empty piece: weight 0
+      W += w;
+      const float4* po = reinterpret_cast<const float4*>(p.ws_o + mslot(i) * kD + 64 * half);
+      float4 o4[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) o4[c] = __ldcg(po + c);
+      if (w == 0.f) return;   // (an empty piece's o was never written)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        acc[4 * c] = fmaf(w, o4[c].x, acc[4 * c]);
+        acc[4 * c + 1] = fmaf(w, o4[c].y, acc[4 * c + 1]);
+        acc[4 * c + 2] = fmaf(w, o4[c].z, acc[4 * c + 2]);
+        acc[4 * c + 3] = fmaf(w, o4[c].w, acc[4 * c + 3]);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kMaxP; ++i)
+      if (i < n_pieces) add_piece(ml[i], i);
+    for (int i = kMaxP; i < n_pieces; ++i) add_piece(__ldcg(&p.ws_ml[mslot(i)]), i);
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(n0 + mln) * p.Hq + mhead) * kD + 64 * half;
+#pragma unroll
+    for (int c = 0; c < 64; c += 8) {
+      const uint4 v4 = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv), pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
+                                  pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
+      *reinterpret_cast<uint4*>(op + c) = v4;
+    }
+    if (half == 0 && p.lse)
+      p.lse[static_cast<int64_t>(n0 + mln) * p.Hq + mhead] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int LIVE>
 __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn_tc_kernel(
@@ -530,60 +590,430 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols) : "memory");
   }
   if (n_pieces > 1 && *last_flag) {
-    // merge in piece order: all threads, two per query row (64 columns each)
-    constexpr int kMaxP = 8;   // weights held in registers; more pieces recompute them
     __threadfence();
-    for (int rr = threadIdx.x >> 1; rr < LIVE; rr += kThreads / 2) {
-      const int mln = node_first + rr / g;
-      if (mln >= cnt) continue;
-      const int mhead = kvh * g + rr % g;
-      const int half = threadIdx.x & 1;
-      auto mslot = [&](int pc) {
-        return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + mln) * p.Hq +
-               mhead;
-      };
-      float2 ml[kMaxP];
-#pragma unroll
-      for (int i = 0; i < kMaxP; ++i) ml[i] = i < n_pieces ? __ldcg(&p.ws_ml[mslot(i)]) : make_float2(-INFINITY, 0.f);
-      float M = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kMaxP; ++i) M = fmaxf(M, ml[i].x);
-      for (int i = kMaxP; i < n_pieces; ++i) M = fmaxf(M, __ldcg(&p.ws_ml[mslot(i)].x));
-      float W = 0.f;
-      float acc[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-      auto add_piece = [&](float2 mi, int i) {
-        const float w = mi.y > 0.f ? ex2(mi.x - M) * mi.y : 0.f;   // empty piece: weight 0
-        W += w;
-        const float4* po = reinterpret_cast<const float4*>(p.ws_o + mslot(i) * kD + 64 * half);
-        float4 o4[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) o4[c] = __ldcg(po + c);
-        if (w == 0.f) return;   // (an empty piece's o was never written)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          acc[4 * c] = fmaf(w, o4[c].x, acc[4 * c]);
-          acc[4 * c + 1] = fmaf(w, o4[c].y, acc[4 * c + 1]);
-          acc[4 * c + 2] = fmaf(w, o4[c].z, acc[4 * c + 2]);
-          acc[4 * c + 3] = fmaf(w, o4[c].w, acc[4 * c + 3]);
-        }
-      };
-#pragma unroll
-      for (int i = 0; i < kMaxP; ++i)
-        if (i < n_pieces) add_piece(ml[i], i);
-      for (int i = kMaxP; i < n_pieces; ++i) add_piece(__ldcg(&p.ws_ml[mslot(i)]), i);
-      const float inv = W > 0.f ? 1.f / W : 0.f;
-      uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(n0 + mln) * p.Hq + mhead) * kD + 64 * half;
-#pragma unroll
-      for (int c = 0; c < 64; c += 8) {
-        const uint4 v4 = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv), pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
-                                    pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
-        *reinterpret_cast<uint4*>(op + c) = v4;
-      }
-      if (half == 0 && p.lse)
-        p.lse[static_cast<int64_t>(n0 + mln) * p.Hq + mhead] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+    merge_pieces<LIVE>(p, r, n0, node_first, cnt, g, kvh, n_pieces, kThreads);
+  }
+}
+
+// ------------------------------------------------------------------ 128-row tiles, 128-key blocks
+// Tiles of 128 query rows (nodes x the group's heads) take keys in blocks of
+// 128: S = Q K^T is one M = 128, N = 128 MMA per 16 dimensions (the N = 64
+// shape costs the same issue time for half the keys), O += P V one M = 128,
+// N = 128 MMA per 16 keys.  Tensor memory (512 columns): S0 | S1 | O | Q; Q
+// and P are tensor-memory A operands, so the MMAs read only K and V from
+// shared memory (rings of 3 K and 2 V blocks of 32 KB).
+//   warp 0   TMA producer: Q once, then K and V blocks, each slot refilled
+//            as soon as the MMA that read it has completed.
+//   warp 1   MMA issuer (event loop): S(j) into buffer j & 1 once K(j) is in
+//            and PV(j - 2) has completed (P(j - 2) lived in that buffer),
+//            PV(j) once P(j) and V(j) are in; S(j + 1) runs while the
+//            softmax warps work on block j.
+//   warps 2-5 softmax, one thread per row (its TMEM lane): the 128 scores of
+//            the block in registers, mask, online base-2 softmax with lazy
+//            rescaling of O in tensor memory (only when the maximum grows by
+//            more than 2^8; O must then be complete: PV(j - 1)), P as bf16
+//            into the first 64 columns of S(j)'s buffer.
+constexpr int kBlk2 = 128;                     // keys per block
+constexpr uint32_t kHalf2 = kBlk2 * 128;       // 128 rows (keys or queries) x 64 dims bf16
+struct Lay2 {
+  static constexpr int kThreads = 192;
+  static constexpr int kTmaWarp = 0, kMmaWarp = 1;
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr uint32_t kQOff = 0;                                   // Q staging: two halves
+  static constexpr uint32_t kKOff = kQOff + 2 * kHalf2;                  // K ring
+  static constexpr uint32_t kVOff = kKOff + kKStages * 2 * kHalf2;       // V ring
+  static constexpr uint32_t kBarOff = kVOff + kVStages * 2 * kHalf2;
+  static constexpr uint32_t kTmemSlot = kBarOff + 8 * 24;
+  static constexpr uint32_t kAbortSlot = kTmemSlot + 4;
+  static constexpr uint32_t kRedSlot = kTmemSlot + 8;                    // [6 warps][3] ints (72 B)
+  static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;
+  static constexpr uint32_t kTmemCols = 512;                             // S0 | S1 | O | Q
+  static_assert(kRedSlot + 72 <= kBarOff + 512, "barrier area");
+};
+// mbarrier slots: K_FULL/K_EMPTY per K stage, V_FULL/V_EMPTY per V stage,
+// S_FULL/P_FULL/PV_DONE per S buffer
+enum Bar2 { B2_Q = 0, B2_QT = 1, B2_K_FULL = 2, B2_K_EMPTY = 5, B2_V_FULL = 8, B2_V_EMPTY = 10, B2_S_FULL = 12,
+            B2_P_FULL = 14, B2_PV_DONE = 16, B2_DRAIN = 18, B2_N = 19 };
+
+__global__ void __launch_bounds__(Lay2::kThreads, 1) attn_tc128_kernel(const __grid_constant__ TcParams P) {
+  using L = Lay2;
+  constexpr int kThreads = L::kThreads;
+  constexpr int LIVE = 128;
+  constexpr int KS = L::kKStages, VS = L::kVStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const AttnParams& p = P.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_release();
+  const int kvh = blockIdx.x, tile = blockIdx.y;
+  const int4 unit = p.plan[blockIdx.z];
+  const int r = unit.x;
+  if (r < 0) return;                                   // uniform: a unit without work
+  const int piece = unit.y, n_pieces = unit.z;
+  const int g = p.Hq / p.Hkv;
+  const int nq = LIVE / g;
+  const int n0 = p.node_off[r];
+  const int N = p.node_off[r + 1] - n0;
+  const int cnt = min(p.node_cnt ? min(p.node_cnt[r], N) : N, p.max_nodes);
+  const int node_first = tile * nq;
+  if (node_first >= cnt) return;                       // uniform: nothing to do
+  const int pre0 = p.pre_off[r];
+  const int Pr = p.pre_off[r + 1] - pre0;
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbortSlot);
+  int* red = reinterpret_cast<int*>(sm + L::kRedSlot);
+  auto bar = [&](int i) { return sb + L::kBarOff + 8u * i; };
+
+  // ---- row identity (softmax warps 2..5 own TMEM lanes 32*(warp%4) ..)
+  const bool is_soft = warp >= 2;
+  const int row = 32 * (warp & 3) + lane;
+  const int ln = node_first + row / g;
+  const int head = kvh * g + row % g;
+  const bool active = is_soft && ln < cnt;
+  const int gn = n0 + ln;
+  int vis = 0, lowest = 1 << 30;
+  if (active) {
+    vis = p.vis_prefix ? p.vis_prefix[gn] : Pr;
+    vis = min(max(vis, 0), Pr);
+    for (int w = 0; w < p.anc_words; ++w) {
+      const uint64_t a = p.anc[static_cast<int64_t>(gn) * p.anc_words + w];
+      if (a) { lowest = w * 64 + __ffsll(static_cast<long long>(a)) - 1; break; }
     }
+  }
+  {
+    const int vm = __reduce_max_sync(0xffffffffu, vis);
+    const int lm = __reduce_min_sync(0xffffffffu, lowest);
+    const int hm = __reduce_max_sync(0xffffffffu, active ? ln : -1);
+    if (lane == 0) { red[3 * warp] = vm; red[3 * warp + 1] = lm; red[3 * warp + 2] = hm; }
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B2_N; ++i) {
+      const bool soft_count = i == B2_QT || i == B2_P_FULL || i == B2_P_FULL + 1;
+      mbar_init(bar(i), soft_count ? LIVE : 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == L::kMmaWarp) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sb + L::kTmemSlot),
+                 "r"(L::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + L::kTmemSlot);
+  int vmax = 0, tlo = 1 << 30, thi = -1;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    vmax = max(vmax, red[3 * w]);
+    tlo = min(tlo, red[3 * w + 1]);
+    thi = max(thi, red[3 * w + 2]);
+  }
+
+  // ---- key blocks of this CTA
+  const int kb = piece * p.piece_len;
+  const int ke = min(kb + p.piece_len, vmax);
+  const int n_pre = ke > kb ? (ke - kb + kBlk2 - 1) / kBlk2 : 0;
+  const bool do_tree = (piece == n_pieces - 1) && thi >= 0 && tlo <= thi;
+  auto pslot = [&](int pc) {
+    return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + ln) * p.Hq + head;
+  };
+  const int tb = do_tree ? (tlo & ~(kBlk2 - 1)) : 0;   // two 64-bit ancestor words per block
+  const int n_tree = do_tree ? (thi + 1 - tb + kBlk2 - 1) / kBlk2 : 0;
+  const int nblk = n_pre + n_tree;
+  int* err = P.err;
+
+  const uint32_t sQ = sb + L::kQOff, sK = sb + L::kKOff, sV = sb + L::kVOff;
+  const uint32_t tS0 = tmem, tO = tmem + 2 * kBlk2, tQ = tmem + 2 * kBlk2 + kD;
+
+  if (nblk > 0) {
+    if (warp == L::kTmaWarp) {
+      // ================= TMA producer: K and V rings refill independently
+      if (lane == 0) {
+        mbar_expect_tx(bar(B2_Q), 2 * kHalf2);
+        tma_load_3d(sQ, &P.maps.q, 0, kvh * g, n0 + node_first, bar(B2_Q));
+        tma_load_3d(sQ + kHalf2, &P.maps.q, 64, kvh * g, n0 + node_first, bar(B2_Q));
+        auto where = [&](int j, const CUtensorMap*& mk, const CUtensorMap*& mv) {
+          const bool tree = j >= n_pre;
+          mk = tree ? &P.maps.kt : &P.maps.kp;
+          mv = tree ? &P.maps.vt : &P.maps.vp;
+          return tree ? n0 + tb + (j - n_pre) * kBlk2 : pre0 + kb + j * kBlk2;
+        };
+        int nk = 0, nv = 0;
+        uint64_t since = 0;
+        while (nk < nblk || nv < nblk) {
+          bool prog = false;
+          if (nk < nblk && (nk < KS || mbar_test(bar(B2_K_EMPTY + nk % KS), ((nk / KS) - 1) & 1))) {
+            const CUtensorMap *mk, *mv;
+            const int coord = where(nk, mk, mv);
+            const uint32_t dk = sK + (nk % KS) * 2 * kHalf2;
+            mbar_expect_tx(bar(B2_K_FULL + nk % KS), 2 * kHalf2);
+            tma_load_3d(dk, mk, 0, kvh, coord, bar(B2_K_FULL + nk % KS));
+            tma_load_3d(dk + kHalf2, mk, 64, kvh, coord, bar(B2_K_FULL + nk % KS));
+            ++nk;
+            prog = true;
+          }
+          if (nv < nk && (nv < VS || mbar_test(bar(B2_V_EMPTY + nv % VS), ((nv / VS) - 1) & 1))) {
+            const CUtensorMap *mk, *mv;
+            const int coord = where(nv, mk, mv);
+            const uint32_t dv = sV + (nv % VS) * 2 * kHalf2;
+            mbar_expect_tx(bar(B2_V_FULL + nv % VS), 2 * kHalf2);
+            tma_load_3d(dv, mv, 0, kvh, coord, bar(B2_V_FULL + nv % VS));
+            tma_load_3d(dv + kHalf2, mv, 64, kvh, coord, bar(B2_V_FULL + nv % VS));
+            ++nv;
+            prog = true;
+          }
+          if (prog) since = 0;
+          else if (!still_waiting(since, abort_flag, err, 21)) break;
+        }
+      }
+    } else if (warp == L::kMmaWarp) {
+      // ================= MMA issuer (event loop)
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16(kRows, kBlk2, 0);
+        constexpr uint32_t idO = idesc_bf16(kRows, kD, 1);
+        bool ok = mbar_wait(bar(B2_QT), 0, abort_flag, err, 22);
+        tc_fence_after();
+        int ns = 0, npv = 0;
+        uint64_t since = 0;
+        while (ok && npv < nblk) {
+          bool prog = false;
+          // S buffer ns & 1 is free once PV(ns - 2), which read P from it, has completed
+          if (ns < nblk && mbar_test(bar(B2_K_FULL + ns % KS), (ns / KS) & 1) &&
+              (ns < 2 || mbar_test(bar(B2_PV_DONE + (ns & 1)), ((ns >> 1) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kbase = sK + (ns % KS) * 2 * kHalf2;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              umma_bf16_ts(tS0 + kBlk2 * (ns & 1), tQ + 8 * kk,
+                           sdesc(kbase + (kk >> 2) * kHalf2 + (kk & 3) * 32, 16, 1024), idS, kk > 0);
+            umma_commit(bar(B2_S_FULL + (ns & 1)));
+            umma_commit(bar(B2_K_EMPTY + ns % KS));
+            ++ns;
+            prog = true;
+          }
+          if (npv < ns && mbar_test(bar(B2_P_FULL + (npv & 1)), (npv >> 1) & 1) &&
+              mbar_test(bar(B2_V_FULL + npv % VS), (npv / VS) & 1)) {
+            tc_fence_after();
+            const uint32_t vbase = sV + (npv % VS) * 2 * kHalf2;
+#pragma unroll
+            for (int kk = 0; kk < kBlk2 / 16; ++kk)
+              umma_bf16_ts(tO, tS0 + kBlk2 * (npv & 1) + 8 * kk, sdesc(vbase + kk * 2048, kHalf2, 1024), idO,
+                           (npv > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar(B2_PV_DONE + (npv & 1)));
+            umma_commit(bar(B2_V_EMPTY + npv % VS));
+            ++npv;
+            prog = true;
+          }
+          if (prog) since = 0;
+          else if (!still_waiting(since, abort_flag, err, 23)) ok = false;
+        }
+        // drain: every MMA issued above has completed before TMEM is released
+        umma_commit(bar(B2_DRAIN));
+        mbar_wait(bar(B2_DRAIN), 0, abort_flag, err, 24);
+      }
+    } else {
+      // ================= softmax warps
+      const float c2 = p.scale * kLog2e;
+      const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const bool warp_live = __any_sync(0xffffffffu, active);
+      // this row of Q -> tensor memory, dims (2c, 2c + 1) in column c: the
+      // 128-byte swizzle puts 16-byte chunk c of a row at chunk c ^ (row & 7)
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B2_Q), 0, abort_flag, err, 25));
+      if (ok && warp_live) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t qw[32];
+          const uint8_t* src = sm + L::kQOff + h * kHalf2 + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+            qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
+          }
+          tmem_st32(tQ + lane_off + 32 * h, qw);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B2_QT));
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nblk && ok; ++j) {
+        const int sb2 = j & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B2_S_FULL + sb2), (j >> 1) & 1, abort_flag, err, 26));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tS0 + kBlk2 * sb2;
+        float rs = 0.f, corr = 1.f;
+        bool rescale_row = false;
+        uint32_t pw[64];
+        if (warp_live) {
+          uint32_t xr[4][32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + 32 * q, xr[q]);
+          tmem_ld_wait();
+          // visibility of the 128 keys of block j for this row (bit c of vm[q]: key 32q + c)
+          uint32_t vm[4] = {0u, 0u, 0u, 0u};
+          if (active) {
+            if (j < n_pre) {
+              const int nvis = min(vis, ke) - (kb + j * kBlk2);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int t = nvis - 32 * q;
+                vm[q] = t >= 32 ? 0xffffffffu : (t > 0 ? (1u << t) - 1u : 0u);
+              }
+            } else {
+              const int w = (tb + (j - n_pre) * kBlk2) >> 6;
+              const int64_t a0 = static_cast<int64_t>(gn) * p.anc_words;
+              const uint64_t a = w < p.anc_words ? p.anc[a0 + w] : 0ull;
+              const uint64_t b = w + 1 < p.anc_words ? p.anc[a0 + w + 1] : 0ull;
+              vm[0] = static_cast<uint32_t>(a);
+              vm[1] = static_cast<uint32_t>(a >> 32);
+              vm[2] = static_cast<uint32_t>(b);
+              vm[3] = static_cast<uint32_t>(b >> 32);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pin(xr[q][c]);
+          // masked scores become -inf only in partial blocks
+          if (__any_sync(0xffffffffu, (vm[0] & vm[1] & vm[2] & vm[3]) != 0xffffffffu)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (!((vm[q] >> c) & 1u)) xr[q][c] = __float_as_uint(-INFINITY);
+          }
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(xr[q][c]));
+          const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+          const float mn = fmaxf(m, mloc);
+          const bool grow = mn > m + 8.f;          // also true when m = -inf and mn is finite
+          const float mu = grow ? mn : m;
+          const float msafe = mu == -INFINITY ? 0.f : mu;
+          float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float e0 = ex2(fmaf(__uint_as_float(xr[q][2 * c]), c2, -msafe));
+              const float e1 = ex2(fmaf(__uint_as_float(xr[q][2 * c + 1]), c2, -msafe));
+              sm4[c & 3] += e0 + e1;
+              pw[16 * q + c] = pack_bf16(e0, e1);
+            }
+          rs = (sm4[0] + sm4[1]) + (sm4[2] + sm4[3]);
+          rescale_row = grow && m != -INFINITY;
+          corr = rescale_row ? ex2(m - mu) : 1.f;
+          m = mu;
+        }
+        // O is touched only when this warp must rescale: PV(j - 1) must then have completed
+        if (warp_live && j > 0 && __any_sync(0xffffffffu, rescale_row)) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar(B2_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, err, 27));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + 32 * q, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              pin(o[c]);
+              o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+            }
+            tmem_st32(tO + lane_off + 32 * q, o);
+          }
+        }
+        if (warp_live) {
+          l = l * corr + rs;
+          // P row -> the first 64 columns of S(j)'s buffer (keys 2c, 2c + 1 in column c)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w16[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) w16[c] = pw[16 * q + c];
+            tmem_st16(tS + lane_off + 16 * q, w16);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B2_P_FULL + sb2));
+      }
+      // the last PV has completed before O is read (PV(j) completes in order)
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B2_PV_DONE + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1,
+                                               abort_flag, err, 28));
+      tc_fence_after();
+      // ---- epilogue: O / l
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool write = active && ok;
+      if (warp_live) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + 32 * q, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pin(o[c]);
+          if (write) {
+            if (n_pieces == 1) {
+              uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(gn) * p.Hq + head) * kD + 32 * q;
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v4 = make_uint4(pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv),
+                                      pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv));
+                *reinterpret_cast<uint4*>(op + c) = v4;
+              }
+            } else {
+              float* po = p.ws_o + pslot(piece) * kD + 32 * q;
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(po + c) =
+                    make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                                __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+            }
+          }
+        }
+      }
+      if (write) {
+        if (n_pieces == 1) {
+          if (p.lse) p.lse[static_cast<int64_t>(gn) * p.Hq + head] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          p.ws_ml[pslot(piece)] = make_float2(m, l);
+        }
+      }
+    }
+  } else if (is_soft && active && n_pieces > 1) {
+    // no keys in this piece: an empty partial
+    p.ws_ml[pslot(piece)] = make_float2(-INFINITY, 0.f);
+  }
+  if (n_pieces > 1) __threadfence();   // this thread's partial, before the count below
+  tc_fence_before();
+  __syncthreads();
+  int* last_flag = red;   // the reduction scratch is free again
+  if (n_pieces > 1 && threadIdx.x == 0) {
+    const int old = atomicAdd(&p.piece_cnt[(static_cast<int64_t>(r) * p.Hkv + kvh) * gridDim.y + tile], 1);
+    *last_flag = old == n_pieces - 1;
+  }
+  if (n_pieces > 1) __syncthreads();
+  if (warp == L::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols) : "memory");
+  }
+  if (n_pieces > 1 && *last_flag) {
+    __threadfence();
+    merge_pieces<LIVE>(p, r, n0, node_first, cnt, g, kvh, n_pieces, kThreads);
   }
 }
 
@@ -711,16 +1141,20 @@ void attn_tc_shape(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int n_
   const int live = tc_live(max_nodes, g);
   const int nq = live / g;
   *tiles = (max_nodes + nq - 1) / nq;
-  const long long slots = static_cast<long long>(n_sm) * (live == 64 ? 2 : 1);   // resident CTAs
+  // Units needed before requests are cut into pieces: 64-row tiles fill both
+  // resident CTAs of an SM; 128-row tiles keep the tensor core of an SM busy
+  // alone (the second resident CTA then overlaps their softmax).
+  const long long slots = static_cast<long long>(n_sm) * (live == 64 ? 2 : 1);
+  const int align = live == 64 ? 64 : 128;                       // keys per block
   // Enough (request, KV head, tile) units to fill the resident slots: whole
   // requests, longest first (a piece split costs a partial round trip and a
   // merge, more than the tail it removes).  Fewer: pieces sized so that the
   // units about fill the slots.
   const long long units = static_cast<long long>(B) * Hkv * *tiles;
-  long long L = std::max(64, (max_prefix + 63) / 64 * 64);
+  long long L = std::max(align, (max_prefix + align - 1) / align * align);
   if (units < slots && max_prefix > 512) {
     const long long keys = units * max_prefix;
-    L = std::max<long long>(512, ((keys + slots - 1) / slots + 63) / 64 * 64);
+    L = std::max<long long>(512, ((keys + slots - 1) / slots + align - 1) / align * align);
   }
   long long mp = max_prefix > 0 ? (max_prefix + L - 1) / L : 1;
   while (static_cast<long long>(B) * mp > 65535) {   // grid z limit
@@ -764,9 +1198,41 @@ static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long 
   return launch_pdl(tc::attn_tc_kernel<LIVE>, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
 }
 
+// 128-row tiles: attn_tc128_kernel (128-key blocks, two CTAs per SM)
+static int attn_tc128_launch(const AttnParams& p, long long total_nodes, long long total_prefix, int* err,
+                             cudaStream_t st) {
+  using L = tc::Lay2;
+  if (!smem_limit(tc::attn_tc128_kernel, static_cast<int>(L::kSmemBytes))) return TV_ECUDA;
+  tc::TcParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.a = p;
+  P.err = err;
+  const int g = p.Hq / p.Hkv;
+  const int nq = 128 / g;
+  bool ok = tc::make_map(&P.maps.q, p.q, p.Hq, total_nodes, g, nq) &&
+            tc::make_map(&P.maps.kt, p.k_tree, p.Hkv, total_nodes, 1, tc::kBlk2) &&
+            tc::make_map(&P.maps.vt, p.v_tree, p.Hkv, total_nodes, 1, tc::kBlk2);
+  if (ok && total_prefix > 0) {
+    ok = tc::make_map(&P.maps.kp, p.k_pre, p.Hkv, total_prefix, 1, tc::kBlk2) &&
+         tc::make_map(&P.maps.vp, p.v_pre, p.Hkv, total_prefix, 1, tc::kBlk2);
+  } else if (ok) {
+    P.maps.kp = P.maps.kt;   // never read: no prefix blocks exist
+    P.maps.vp = P.maps.vt;
+  }
+  if (!ok) return TV_ECUDA;
+  const int tiles = (p.max_nodes + nq - 1) / nq;
+  const int n_buckets = static_cast<int>(std::min<long long>(
+      tc::kPlanBuckets, (std::min<long long>(p.piece_len, p.max_prefix) / 64 + 2 + 31) / 32 * 32));
+  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st, p.pre_off, p.B, p.piece_len,
+                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles,
+                      n_buckets, err);
+  if (rc != TV_OK) return rc;
+  return launch_pdl(tc::attn_tc128_kernel, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
+}
+
 int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st) {
   if (tc_live(p.max_nodes, p.Hq / p.Hkv) == 64) return attn_tc_launch<64>(p, total_nodes, total_prefix, err, st);
-  return attn_tc_launch<128>(p, total_nodes, total_prefix, err, st);
+  return attn_tc128_launch(p, total_nodes, total_prefix, err, st);
 }
 
 }  // namespace tv
