@@ -371,6 +371,22 @@ def capture(torch, fn, stream, reps=1):
     return g
 
 
+def capture_seq(torch, fns, stream):
+    """Graph of the calls ``fns`` in order (each called once outside the graph
+    first), e.g. one call per buffer copy so that no call reads what the
+    previous one left in L2."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fns:
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def copies_for(nbytes):
     """Distinct buffer copies needed for a rotation to exceed L2 twice over."""
     return max(1, min(32, math.ceil(2 * L2_BYTES / max(1, nbytes))))
@@ -381,6 +397,17 @@ def attn_bytes(plen, kept, Hq=32, Hkv=8, d=128):
     prefix K/V once, plus q, o and the own K/V row of each verified node."""
     kv = int(plen.sum()) * Hkv * d * 2 * 2
     return kv + int(kept) * (2 * Hq * d * 2 + 2 * Hkv * d * 2)
+
+
+def sfu_ex2_per_s(torch):
+    """Peak rate of 2^x on the special-function units: 16 results per clock
+    per SM (4 per sub-partition) at the maximum SM clock."""
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = 2070.0
+    mp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(mp):
+        mhz = float(json.load(open(mp)).get("sm_max_mhz", mhz))
+    return 16.0 * p.multi_processor_count * mhz * 1e6
 
 
 def row_entry(us, byts, pk, bound="hbm"):
@@ -411,9 +438,19 @@ def measure_rows(tv, torch, pk, stream, only=None):
         mtok = torch.randint(0, V, (1024,), generator=g, device="cuda", dtype=torch.int32)
         ws = torch.empty(tv.load_library().tree_tv_alpha_workspace_size(1024, V), dtype=torch.uint8, device="cuda")
         o3 = tuple(torch.empty(1024, dtype=torch.float32, device="cuda") for _ in range(3))
-        gr = capture(torch, lambda: tv.tree_tv_alpha(lp, lq, boff, mtok, ws=ws, outputs=o3), stream)
-        rows["tree_tv_alpha[specopd 1024x151936 p,q bf16]"] = row_entry(
-            time_graph(torch, gr, 10, stream) * 1e3, 2 * 1024 * V * 2, pk)
+        gr = capture(torch, lambda: tv.tree_tv_alpha(lp, lq, boff, mtok, ws=ws, outputs=o3), stream,
+                     reps=KERNEL_REPS)
+        us = time_graph(torch, gr, 10, stream) * 1e3 / KERNEL_REPS
+        e = row_entry(us, 2 * 1024 * V * 2, pk)
+        # the special-function unit bounds this kernel: three exponentials per
+        # vocabulary entry (the log-sum-exp of p and of q, then 2^min), 16 per
+        # clock per SM
+        n_ex2 = 3 * 1024 * V
+        sfu_peak = sfu_ex2_per_s(torch)
+        e.update(bound="sfu", ex2_per_s=round(n_ex2 / (us * 1e-6) / 1e12, 3), sfu_peak_ex2_per_s=round(sfu_peak / 1e12, 3),
+                 frac_sfu=round(n_ex2 / (us * 1e-6) / sfu_peak, 3), frac_hbm=e["frac"])
+        e["frac"] = e["frac_sfu"]
+        rows["tree_tv_alpha[specopd 1024x151936 p,q bf16]"] = e
         del lp, lq, gr
     # a3: vocab reductions, Graft single request (61 rows) and D-cut batch (1024 rows)
     if want("vocab_argmax_topk"):
@@ -426,9 +463,13 @@ def measure_rows(tv, torch, pk, stream, only=None):
             outs = (torch.empty(R, dtype=torch.int32, device="cuda"), torch.empty((R, 8), dtype=torch.int32, device="cuda"),
                     torch.empty((R, 8), dtype=torch.float32, device="cuda"), torch.empty(R, dtype=torch.float32, device="cuda"),
                     torch.empty(R, dtype=torch.float32, device="cuda"))
-            grs = [capture(torch, lambda L=L: tv.vocab_argmax_topk(L, k=8, ws=wsv, outputs=outs), stream) for L in Ls]
+            # graphs of several consecutive calls (as inside a step), each call
+            # on its own copy of the logits so that none is served from L2
+            reps = KERNEL_REPS if nc == 1 else min(KERNEL_REPS, nc)   # one copy: it exceeds L2 already
+            grs = [capture_seq(torch, [lambda L=Ls[(i * reps + c) % nc]: tv.vocab_argmax_topk(L, k=8, ws=wsv, outputs=outs)
+                                       for c in range(reps)], stream) for i in range(nc)]
             rows[f"vocab_argmax_topk[{R}x151936 bf16, k=8, max+lse]"] = row_entry(
-                time_graph(torch, grs, 10 * nc, stream) * 1e3, R * V * 2, pk)
+                time_graph(torch, grs, 10 * nc, stream) * 1e3 / reps, R * V * 2, pk)
             del Ls, grs
     # a9: BlockPilot MLP (W1 151936 x 2048 bf16 = 622 MB)
     if want("blockpilot_mlp"):
@@ -453,10 +494,12 @@ def measure_rows(tv, torch, pk, stream, only=None):
         nb = torch.zeros(1, dtype=torch.int32, device="cuda")
         wsa = torch.empty(max(256, tv.load_library().graft_adj_update_workspace_size(V, V)), dtype=torch.uint8,
                           device="cuda")
-        grs = [capture(torch, lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb, ws=wsa), stream)
-               for a, t, k in sets]
+        reps = min(KERNEL_REPS, nc)
+        grs = [capture_seq(torch, [lambda a=a, t=t, k=k: tv.graft_adj_update(a, t, k, n_bad=nb, ws=wsa)
+                                   for a, t, k in (sets[(i * reps + c) % nc] for c in range(reps))], stream)
+               for i in range(nc)]
         rows["graft_adj_update[bulk 151936 rows x 8]"] = row_entry(
-            time_graph(torch, grs, 10 * nc, stream) * 1e3, nbytes, pk)
+            time_graph(torch, grs, 10 * nc, stream) * 1e3 / reps, nbytes, pk)
         del sets, grs
     # a2 on the large-tree shapes, against the bf16 tensor peak: the SpecOPD
     # proposal tree (1024 nodes over one 4096-token trunk, 64 anchors) and the

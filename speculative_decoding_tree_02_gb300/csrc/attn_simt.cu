@@ -328,7 +328,9 @@ int attn_simt_splits(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int 
   const long long base = static_cast<long long>(B) * Hkv * tiles;
   const long long target = 4LL * n_sm;   // two resident CTAs per SM, two waves
   long long s = (target + base - 1) / base;
-  const long long cap = std::max(1, (max_prefix + 255) / 256);
+  // splits of at least 64 keys (a short prefix over few tiles is split
+  // finer: its CTAs are latency-bound, the combine costs one small kernel)
+  const long long cap = std::max(1, (max_prefix + 63) / 64);
   s = std::min(s, cap);
   s = std::max(1LL, std::min(s, 64LL));
   return static_cast<int>(s);

@@ -1,17 +1,19 @@
 // tree_verify_attn, tensor-core path (bf16, head_dim 128): tree-masked GQA
 // attention on the 5th-generation tensor cores (Graft page §2 third gear;
-// SpecOPD page §02 proposal-tree scoring with the ancestor mask).
+// SpecOPD page §02 proposal-tree scoring with the ancestor mask).  A tile is
+// a set of query rows = (nodes x the g query heads of one KV head).
 //
-// One CTA = (request, KV head, tile of 128 query rows = 128/g nodes x g heads,
-// split of the prefix keys).  Keys stream in blocks of 64:
-//   warp 0   TMA producer: Q once, then K and V blocks into separate 5-stage
+// 64-row tiles (a request's nodes x heads fit in 64 rows: the D-cut chains):
+// attn_tc_kernel<64>, one CTA = (request, KV head, tile, split of the prefix
+// keys), two CTAs per SM, keys in blocks of 64:
+//   warp 2   TMA producer: Q once, then K and V blocks into separate 2-stage
 //            rings (cp.async.bulk.tensor, 128-byte swizzle): a K slot is
 //            reused once S of its block is done, a V slot once PV is.
-//   warp 1   MMA issuer (one thread, event loop): S = Q K^T into a double-buffered TMEM
-//            accumulator (128 x 64 fp32), then O += P V into a TMEM
-//            accumulator (128 x 128 fp32); tcgen05.commit signals mbarriers.
-//            Also owns the TMEM allocation (256 columns).
-//   warps 2-5 softmax, one thread per query row (its TMEM lane): load S,
+//   warp 3   MMA issuer (one thread, event loop): S = Q K^T into a
+//            double-buffered TMEM accumulator (128 x 64 fp32), then O += P V
+//            into a TMEM accumulator (128 x 128 fp32); tcgen05.commit
+//            signals mbarriers.  Also owns the TMEM allocation (256 columns).
+//   warps 0-1 softmax, one thread per query row (its TMEM lane): load S,
 //            apply the ancestor/prefix mask in registers, online base-2
 //            softmax with lazy rescaling (O is rescaled in TMEM only when the
 //            running max grows by more than 2^8), write P as bf16 into shared
@@ -22,6 +24,9 @@
 // buffer), and for PV(j-1) only in the rare block where O must be rescaled,
 // so the tensor core and the softmax warps overlap across blocks.
 // S for block j+1 is computed while the softmax warps work on block j.
+//
+// 128-row tiles: attn_tc128_kernel (below), keys in blocks of 128.
+//
 // Every wait is bounded (2 s): on expiry the CTA records an error code in the
 // workspace status word and stops; TMEM is always released.
 #include <cuda.h>
@@ -43,22 +48,21 @@ constexpr int kD = 128;
 constexpr uint32_t kKVHalf = 8192;           // 64 keys x 64 dims bf16
 
 
-// Shared-memory layout for LIVE query rows per tile (128, or 64 when a
-// request's nodes x heads fit in 64 rows).  The MMA always has M = 128; with
-// LIVE = 64 its rows 64..127 read the bytes that follow Q or P (still inside
-// the CTA's shared memory) and the results of those rows are never used.  The
-// 64-row layout is half the size, so two CTAs share an SM.
+// Shared-memory layout for 64-row tiles.  The MMA always has M = 128: its
+// rows 64..127 read the bytes that follow Q or P (still inside the CTA's
+// shared memory) and the results of those rows are never used.  The layout
+// is small enough for two CTAs per SM.
 template <int LIVE>
 struct Lay {
-  // warp roles: softmax warps own TMEM lanes 32*(warp%4)..; with 64 live rows
-  // only lanes 0..63 matter, so the CTA is 4 warps (softmax 0-1, TMA 2, MMA 3);
-  // with 128 it is 6 warps (TMA 0, MMA 1, softmax 2-5)
-  static constexpr int kThreads = LIVE == 128 ? 192 : 128;
+  static_assert(LIVE == 64, "128-row tiles run attn_tc128_kernel");
+  // warp roles: softmax warps own TMEM lanes 32*(warp%4)..; only lanes 0..63
+  // matter, so the CTA is 4 warps (softmax 0-1, TMA 2, MMA 3)
+  static constexpr int kThreads = 128;
   static constexpr int kSoft = LIVE;                     // softmax threads
-  static constexpr int kTmaWarp = LIVE == 128 ? 0 : 2;
-  static constexpr int kMmaWarp = LIVE == 128 ? 1 : 3;
-  static __device__ __forceinline__ bool soft_warp(int w) { return LIVE == 128 ? w >= 2 : w < 2; }
-  static constexpr int kStages = LIVE == 128 ? 5 : 2;   // per ring (K and V)
+  static constexpr int kTmaWarp = 2;
+  static constexpr int kMmaWarp = 3;
+  static __device__ __forceinline__ bool soft_warp(int w) { return w < 2; }
+  static constexpr int kStages = 2;                      // per ring (K and V)
   static constexpr uint32_t kQHalf = LIVE * 128;        // LIVE rows x 64 dims
   static constexpr uint32_t kPBytes = LIVE * 128;       // LIVE rows x 64 keys
   static constexpr uint32_t kQOff = 0;
@@ -71,18 +75,14 @@ struct Lay {
   static constexpr uint32_t kAbortSlot = kTmemSlot + 4;
   static constexpr uint32_t kRedSlot = kTmemSlot + 8;   // [6 warps][3] ints (72 B)
   static_assert(kRedSlot + 72 <= kBarOff + 512, "barrier area");
-  // 128 live rows (one CTA per SM): Q and P are tensor-memory A operands, so
-  // the MMAs read only K and V from shared memory.  TMEM: S0 | S1 | O | Q
-  // (P(j) overwrites the first 32 columns of S(j) once they are read).
-  // 64 live rows (two CTAs per SM, 256 columns each): S0 | S1 | O, Q and P
-  // in shared memory.
-  static constexpr bool kTmemAB = LIVE == 128;
-  static constexpr uint32_t kTmemCols = kTmemAB ? 512 : 256;
+  // TMEM (256 columns per CTA, two CTAs per SM): S0 | S1 | O; Q and P in
+  // shared memory.
+  static constexpr uint32_t kTmemCols = 256;
 };
 
 // mbarrier slots (8 bytes each) at kBarOff; K/V arrays sized for 5 stages
 enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 6, K_EMPTY = 11, V_EMPTY = 16, S_FULL = 21, S_FREE = 23,
-           P_FULL = 25, P_FREE = 27, O_READY = 29, DRAIN = 30, Q_TMEM = 31, N_BARS = 32 };
+           P_FULL = 25, P_FREE = 27, O_READY = 29, DRAIN = 30, N_BARS = 31 };
 
 struct Maps {
   CUtensorMap q, kp, vp, kt, vt;
@@ -156,7 +156,7 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, int r, int n0,
 
 // ------------------------------------------------------------------ kernel
 template <int LIVE>
-__global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn_tc_kernel(
+__global__ void __launch_bounds__(Lay<LIVE>::kThreads, 2) attn_tc_kernel(
     const __grid_constant__ TcParams P) {
   using L = Lay<LIVE>;
   constexpr int kThreads = L::kThreads;
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
   if (threadIdx.x == 0) {
     for (int i = 0; i < N_BARS; ++i) {
       uint32_t c = 1;
-      if (i == S_FREE || i == S_FREE + 1 || i == P_FULL || i == P_FULL + 1 || i == Q_TMEM) c = L::kSoft;
+      if (i == S_FREE || i == S_FREE + 1 || i == P_FULL || i == P_FULL + 1) c = L::kSoft;
       mbar_init(bar(i), c);
     }
     *abort_flag = 0;
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
   int* err = P.err;
 
   const uint32_t sQ = sb + L::kQOff, sP = sb + L::kPOff, sK = sb + L::kKRingOff, sV = sb + L::kVRingOff;
-  const uint32_t tS0 = tmem, tO = tmem + 2 * kBlk, tQ = tmem + 2 * kBlk + kD;
+  const uint32_t tS0 = tmem, tO = tmem + 2 * kBlk;
 
   if (nblk > 0) {
     if (warp == L::kTmaWarp) {
@@ -303,27 +303,22 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16(kRows, kBlk, 0);
         constexpr uint32_t idO = idesc_bf16(kRows, kD, 1);
-        bool ok = mbar_wait(bar(L::kTmemAB ? Q_TMEM : Q_FULL), 0, abort_flag, err, 2);
+        bool ok = mbar_wait(bar(Q_FULL), 0, abort_flag, err, 2);
         tc_fence_after();
         int ns = 0, npv = 0;
         uint64_t since = 0;
         while (ok && npv < nblk) {
           bool prog = false;
-          // S buffer ns&1 is free once its previous S was read (and, with P in
-          // tensor memory, once the PV that read P from it has completed)
+          // S buffer ns&1 is free once its previous S was read
           if (ns < nblk && mbar_test(bar(K_FULL + ns % kStages), (ns / kStages) & 1) &&
-              (ns < 2 || mbar_test(bar((L::kTmemAB ? P_FREE : S_FREE) + (ns & 1)), ((ns >> 1) - 1) & 1))) {
+              (ns < 2 || mbar_test(bar(S_FREE + (ns & 1)), ((ns >> 1) - 1) & 1))) {
             tc_fence_after();
             const uint32_t kbase = sK + (ns % kStages) * 2 * kKVHalf;
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               const uint32_t ko = (kk >> 2) * kKVHalf + (kk & 3) * 32;
-              if constexpr (L::kTmemAB) {
-                umma_bf16_ts(tS0 + kBlk * (ns & 1), tQ + 8 * kk, sdesc(kbase + ko, 16, 1024), idS, kk > 0);
-              } else {
-                const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                umma_bf16(tS0 + kBlk * (ns & 1), sdesc(sQ + qo, 16, 1024), sdesc(kbase + ko, 16, 1024), idS, kk > 0);
-              }
+              const uint32_t qo = (kk >> 2) * kQHalf + (kk & 3) * 32;
+              umma_bf16(tS0 + kBlk * (ns & 1), sdesc(sQ + qo, 16, 1024), sdesc(kbase + ko, 16, 1024), idS, kk > 0);
             }
             umma_commit(bar(S_FULL + (ns & 1)));
             umma_commit(bar(K_EMPTY + ns % kStages));
@@ -337,15 +332,11 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
             const uint32_t pbase = sP + (npv & 1) * kPBytes;
 #pragma unroll
             for (int kk = 0; kk < kBlk / 16; ++kk) {
-              // P: K-major over the 64 keys (one 128-byte swizzle column, or 8
-              // tensor-memory columns per 16 keys); V: MN-major, 16 keys = two
-              // 1 KB atoms, second 64-dim half kKVHalf bytes away
-              if constexpr (L::kTmemAB)
-                umma_bf16_ts(tO, tS0 + kBlk * (npv & 1) + 8 * kk, sdesc(vbase + kk * 2048, kKVHalf, 1024), idO,
-                             (npv > 0 || kk > 0) ? 1u : 0u);
-              else
-                umma_bf16(tO, sdesc(pbase + kk * 32, 16, 1024), sdesc(vbase + kk * 2048, kKVHalf, 1024), idO,
-                          (npv > 0 || kk > 0) ? 1u : 0u);
+              // P: K-major over the 64 keys (one 128-byte swizzle column); V:
+              // MN-major, 16 keys = two 1 KB atoms, second 64-dim half kKVHalf
+              // bytes away
+              umma_bf16(tO, sdesc(pbase + kk * 32, 16, 1024), sdesc(vbase + kk * 2048, kKVHalf, 1024), idO,
+                        (npv > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(bar(P_FREE + (npv & 1)));
             umma_commit(bar(O_READY));
@@ -366,28 +357,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
       const bool warp_live = __any_sync(0xffffffffu, active);
       uint8_t* prow = sm + L::kPOff + row * 128;
-      if constexpr (L::kTmemAB) {
-        // this row of Q -> tensor memory, dims (2c, 2c+1) in column c: the
-        // 128-byte swizzle puts 16-byte chunk c of a row at chunk c ^ (row & 7)
-        bool okq = __all_sync(0xffffffffu, mbar_wait(bar(Q_FULL), 0, abort_flag, err, 12));
-        if (okq && warp_live) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t qw[32];
-            const uint8_t* src = sm + L::kQOff + h * kQHalf + row * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
-              qw[4 * c] = v.x; qw[4 * c + 1] = v.y; qw[4 * c + 2] = v.z; qw[4 * c + 3] = v.w;
-            }
-            tmem_st32(tQ + lane_off + 32 * h, qw);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(Q_TMEM));
-      }
-      if (!L::kTmemAB && !warp_live && row < LIVE) {
+      if (!warp_live && row < LIVE) {
         // rows that are no live query: P stays zero in both buffers for the whole CTA
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -500,24 +470,15 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, LIVE == 128 ? 1 : 2) attn
             tmem_st_wait();
           }
           l = l * corr + rs;
-          if constexpr (L::kTmemAB) {
-            // P row -> the first 32 columns of S(j)'s buffer (keys 2c, 2c+1 in column c)
-            uint32_t pw[32];
+          // P row -> shared memory, K-major 128-byte swizzle (8 chunks of 8 keys)
+          uint8_t* pdst = prow + (j & 1) * kPBytes;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) { pw[c] = pk[0][c]; pw[16 + c] = pk[1][c]; }
-            tmem_st32(tS0 + kBlk * sb2 + lane_off, pw);
-            tmem_st_wait();
-          } else {
-            // P row -> shared memory, K-major 128-byte swizzle (8 chunks of 8 keys)
-            uint8_t* pdst = prow + (j & 1) * kPBytes;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              const uint32_t* src = &pk[c8 >> 2][(c8 & 3) * 4];
-              *reinterpret_cast<uint4*>(pdst + ((c8 ^ (row & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
-            }
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint32_t* src = &pk[c8 >> 2][(c8 & 3) * 4];
+            *reinterpret_cast<uint4*>(pdst + ((c8 ^ (row & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
           }
         }
-        if constexpr (!L::kTmemAB) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         mbar_arrive(bar(P_FULL + (j & 1)));
       }

@@ -796,8 +796,9 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
   const int n_chunks = (V + kVChunk - 1) / kVChunk;
   const bool vec_ok = aligned(logits, 16) && ((ld * static_cast<int64_t>(sizeof(T))) % 16 == 0);
   auto* part = reinterpret_cast<VocabPart<KMAX>*>(ws);
-  // the streaming kernel's bulk copies need 16-byte rows and chunk tails
-  const bool stream_ok = vec_ok && (static_cast<int64_t>(V) * sizeof(T)) % 16 == 0;
+  // the streaming kernel's bulk copies need 16-byte rows and chunk tails; rows
+  // of one chunk are reduced whole by one CTA each (the partial kernels below)
+  const bool stream_ok = vec_ok && (static_cast<int64_t>(V) * sizeof(T)) % 16 == 0 && n_chunks > 1;
   if (stream_ok) {
     constexpr int smem = stream_stages<T>() * stream_chunk_bytes<T>();
     if (!smem_limit(vocab_stream_kernel<T, LSE>, smem)) return TV_ECUDA;

@@ -677,3 +677,18 @@ def test_vocab_status_word_clear_after_a_normal_call(tv):
     assert int(ws[:4].view(torch.int32).item()) == 0
     assert np.array_equal(host(am), ovoc.argmax_topk(x, 1)[0])
 
+
+
+@pytest.mark.parametrize("sizes,P", [([80, 40, 1, 33], 700), ([96], 3000), ([200, 130], 257)])
+def test_attn_128_row_tiles_ragged(tv, sizes, P):
+    """128-row tiles with 128-key blocks: several tiles per request, ragged
+    last tiles, a one-node request, and key pieces with their merge (few
+    tiles over a long prefix)."""
+    rng = synth.make_rng(61, len(sizes) * 1000 + P)
+    parent = np.concatenate([synth.random_tree(rng, n, 9) for n in sizes])
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    plen = rng.integers(P // 2, P + 1, len(sizes)).astype(np.int32)
+    att = synth.attention_tensors(rng, int(off[-1]), int(plen.sum()), 32, 8, 128, "bf16")
+    d = dict(parent=parent, node_off=off, pre_off=np.concatenate([[0], np.cumsum(plen)]).astype(np.int32),
+             vis_prefix=None, dtype="bf16", **att)
+    run_attn(tv, d)
