@@ -26,11 +26,12 @@ struct AttnParams {
   int B, max_nodes, max_prefix, Hq, Hkv, d, dtype;
   float scale;
   int n_split;
-  // Tensor-core work plan: unit z of the grid covers keys [piece * piece_len,
-  // (piece + 1) * piece_len) of request r, the last piece also the tree
-  // block; the pieces of one (request, KV head, tile) are merged by the last
-  // of them to finish.  Units are ordered longest first.
-  const int4* plan;    // [n_units] (r, piece, n_pieces, 0); r < 0: no work
+  // Tensor-core work plan: entry u (grid position z * tiles + y) covers keys
+  // [piece * piece_len, (piece + 1) * piece_len) of node tile t of request r,
+  // the last piece also the tile's tree keys; the pieces of one (request, KV
+  // head, tile) are merged by the last of them to finish.  Entries are
+  // ordered longest first.
+  const int4* plan;    // [n_units] (r, piece, n_pieces, t); r < 0: no work
   int* piece_cnt;      // [B * Hkv * tiles] finished pieces, zeroed by the planner
   int piece_len;       // keys per piece, a multiple of 64
   int n_units;

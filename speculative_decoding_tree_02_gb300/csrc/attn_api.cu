@@ -46,7 +46,7 @@ WsLayout ws_layout(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int d,
   if (w.tc) {
     tv::attn_tc_shape(B, max_nodes, max_prefix, Hq, Hkv, sm_count(), &w.piece_len, &w.max_pieces, &w.tiles);
     w.n_split = 1;
-    w.n_units = B * w.max_pieces;
+    w.n_units = B * w.tiles * w.max_pieces;   // (request, tile, piece) plan entries
     w.plan = align256(static_cast<size_t>(w.n_units) * sizeof(int4));
     w.cnt = align256(static_cast<size_t>(B) * Hkv * w.tiles * sizeof(int));
     if (w.max_pieces > 1) parts = static_cast<size_t>(w.max_pieces) * B * max_nodes * Hq;

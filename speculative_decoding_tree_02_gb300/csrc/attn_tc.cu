@@ -169,11 +169,11 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, 2) attn_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
   griddep_release();
-  const int kvh = blockIdx.x, tile = blockIdx.y;
-  const int4 unit = p.plan[blockIdx.z];
+  const int kvh = blockIdx.x;
+  const int4 unit = p.plan[static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y];   // plan order
   const int r = unit.x;
   if (r < 0) return;                                   // uniform: a unit without work
-  const int piece = unit.y, n_pieces = unit.z;
+  const int piece = unit.y, n_pieces = unit.z, tile = unit.w;
   const int g = p.Hq / p.Hkv;
   const int nq = LIVE / g;
   const int n0 = p.node_off[r];
@@ -608,11 +608,11 @@ __global__ void __launch_bounds__(Lay2::kThreads, 1) attn_tc128_kernel(const __g
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
   griddep_release();
-  const int kvh = blockIdx.x, tile = blockIdx.y;
-  const int4 unit = p.plan[blockIdx.z];
+  const int kvh = blockIdx.x;
+  const int4 unit = p.plan[static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y];   // plan order
   const int r = unit.x;
   if (r < 0) return;                                   // uniform: a unit without work
-  const int piece = unit.y, n_pieces = unit.z;
+  const int piece = unit.y, n_pieces = unit.z, tile = unit.w;
   const int g = p.Hq / p.Hkv;
   const int nq = LIVE / g;
   const int n0 = p.node_off[r];
@@ -978,46 +978,74 @@ __global__ void __launch_bounds__(Lay2::kThreads, 1) attn_tc128_kernel(const __g
   }
 }
 
-// Work plan (one CTA): request r gets n_r = max(1, ceil(P_r / piece_len))
-// pieces.  Units [0, F) are the full pieces (length piece_len) of every
-// request in (r, piece) order, F = sum (n_r - 1); units [F, F + B) are the
-// last pieces by decreasing length (64-key buckets; order within a bucket is
-// free: the merge runs in piece order whatever the schedule); the rest have
-// no work.  Also zeroes the status word and the piece counters.
+// Work plan (one CTA).  A unit is (request r, node tile t, piece): tile t
+// of request r sees keys up to V_rt = the largest visible prefix among its
+// nodes (the request's prefix without per-node prefixes) and takes
+// n_rt = max(1, ceil(V_rt / piece_len)) pieces, the last of which also
+// covers the tile's tree keys.  Units are placed in decreasing order of
+// their prefix keys (64-key buckets; order within a bucket is free: the
+// merge runs in piece order whatever the schedule), so the grid, which
+// dispatches plan entries in order, runs the longest first.  Entries past
+// the units have no work.  Also zeroes the status word and the piece
+// counters.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 1024;
-__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* __restrict__ pre_off, int B,
-                                                                 int piece_len, int max_pieces, int n_units,
-                                                                 int4* __restrict__ plan,
-                                                                 int* __restrict__ piece_cnt, int n_cnt,
-                                                                 int n_buckets, int* __restrict__ status) {
-  __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets], s_w[33];
-  __shared__ int s_base;
+struct PlanArgs {
+  const int32_t* pre_off;
+  const int32_t* node_off;
+  const int32_t* node_cnt;
+  const int32_t* vis_prefix;
+  int B, max_nodes, nq, tiles, piece_len, max_pieces, n_units, n_buckets;
+  int4* plan;
+  int* piece_cnt;
+  int n_cnt;
+  int* status;
+};
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const PlanArgs a) {
+  __shared__ int s_hist[kPlanBuckets], s_fill[kPlanBuckets];
+  __shared__ int s_total;
   griddep_wait();
   griddep_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) { *status = 0; s_base = 0; }
-  for (int i = tid; i < n_cnt; i += kPlanThreads) piece_cnt[i] = 0;
-  for (int i = tid; i < n_buckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
+  if (tid == 0) *a.status = 0;
+  for (int i = tid; i < a.n_cnt; i += kPlanThreads) a.piece_cnt[i] = 0;
+  for (int i = tid; i < a.n_buckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
   __syncthreads();
-  auto shape = [&](int r, int& n, int& bucket) {
-    const int Pr = pre_off[r + 1] - pre_off[r];
-    n = Pr > 0 ? min((Pr + piece_len - 1) / piece_len, max_pieces) : 1;   // keys past max_prefix: none
-    const int last = Pr - (n - 1) * piece_len;
-    bucket = min(n_buckets - 1, (last + 63) / 64);
+  const int L = a.piece_len;
+  // pieces of tile t of request r and its visible keys; false: no nodes
+  auto tile_shape = [&](int r, int t, int& n, int& vk) {
+    const int n0 = a.node_off[r];
+    const int N = a.node_off[r + 1] - n0;
+    const int cnt = min(a.node_cnt ? min(a.node_cnt[r], N) : N, a.max_nodes);
+    const int first = t * a.nq;
+    if (first >= cnt) return false;
+    const int Pr = a.pre_off[r + 1] - a.pre_off[r];
+    vk = Pr;
+    if (a.vis_prefix) {
+      vk = 0;
+      for (int i = first; i < min(first + a.nq, cnt); ++i) vk = max(vk, min(max(a.vis_prefix[n0 + i], 0), Pr));
+    }
+    n = vk > 0 ? min((vk + L - 1) / L, a.max_pieces) : 1;
+    return true;
   };
-  for (int r = tid; r < B; r += kPlanThreads) {
-    int n, bk;
-    shape(r, n, bk);
-    atomicAdd(&s_hist[bk], 1);
+  auto bucket = [&](int vk, int n, int pc) {
+    const int keys = pc < n - 1 ? L : vk - (n - 1) * L;
+    return min(a.n_buckets - 1, (keys + 63) / 64);
+  };
+  const int pairs = a.B * a.tiles;
+  for (int e = tid; e < pairs; e += kPlanThreads) {
+    int n, vk;
+    if (!tile_shape(e / a.tiles, e % a.tiles, n, vk)) continue;
+    for (int pc = 0; pc < n; ++pc) atomicAdd(&s_hist[bucket(vk, n, pc)], 1);
   }
   __syncthreads();
   // bucket starts in decreasing-length order (one warp, suffix sums)
   if (warp == 0) {
     int carry = 0;
-    for (int b0 = n_buckets - 32; b0 >= 0; b0 -= 32) {
+    for (int b0 = a.n_buckets - 32; b0 >= 0; b0 -= 32) {
       const int b = b0 + 31 - lane;          // lane 0 takes the longest bucket of the group
-      int v = s_hist[b], x = v;
+      const int v = s_hist[b];
+      int x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -1026,51 +1054,45 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const int32_t* 
       s_fill[b] = carry + x - v;             // units of longer buckets before this one
       carry += __shfl_sync(0xffffffffu, x, 31);
     }
+    if (lane == 0) s_total = carry;
   }
   __syncthreads();
-  // full pieces: exclusive scan of (n_r - 1) over requests, in chunks of the block
-  for (int r0 = 0; r0 < B; r0 += kPlanThreads) {
-    const int r = r0 + tid;
-    int n = 1, bk = 0;
-    if (r < B) shape(r, n, bk);
-    const int full = n - 1;
-    int x = full;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+  for (int e = tid; e < pairs; e += kPlanThreads) {
+    const int r = e / a.tiles, t = e % a.tiles;
+    int n, vk;
+    if (!tile_shape(r, t, n, vk)) continue;
+    for (int pc = 0; pc < n; ++pc) {
+      const int bk = bucket(vk, n, pc);
+      const int pos = s_fill[bk] + atomicAdd(&s_hist[bk], -1) - 1;   // any slot of the bucket
+      a.plan[pos] = make_int4(r, pc, n, t);
     }
-    if (lane == 31) s_w[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      const int w = s_w[lane];
-      int iw = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, iw, o);
-        if (lane >= o) iw += y;
-      }
-      s_w[lane] = iw - w;
-      if (lane == 31) s_w[32] = iw;
-    }
-    __syncthreads();
-    const int start = s_base + s_w[warp] + x - full;
-    for (int pc = 0; pc < full; ++pc) plan[start + pc] = make_int4(r, pc, n, 0);
-    __syncthreads();
-    if (tid == 0) s_base += s_w[32];
-    __syncthreads();
   }
-  const int F = s_base;
-  for (int r = tid; r < B; r += kPlanThreads) {
-    int n, bk;
-    shape(r, n, bk);
-    const int pos = F + s_fill[bk] + atomicAdd(&s_hist[bk], -1) - 1;   // any slot of the bucket
-    plan[pos] = make_int4(r, n - 1, n, 0);
-  }
-  for (int u = F + B + tid; u < n_units; u += kPlanThreads) plan[u] = make_int4(-1, 0, 0, 0);
+  __syncthreads();
+  for (int u = s_total + tid; u < a.n_units; u += kPlanThreads) a.plan[u] = make_int4(-1, 0, 0, 0);   // no work
 }
 
 // ------------------------------------------------------------------ host side
+PlanArgs plan_args(const AttnParams& p, int nq, int tiles, int n_buckets, int* err) {
+  PlanArgs a;
+  a.pre_off = p.pre_off;
+  a.node_off = p.node_off;
+  a.node_cnt = p.node_cnt;
+  a.vis_prefix = p.vis_prefix;
+  a.B = p.B;
+  a.max_nodes = p.max_nodes;
+  a.nq = nq;
+  a.tiles = tiles;
+  a.piece_len = p.piece_len;
+  a.max_pieces = p.n_units / (p.B * tiles);
+  a.n_units = p.n_units;
+  a.n_buckets = n_buckets;
+  a.plan = const_cast<int4*>(p.plan);
+  a.piece_cnt = p.piece_cnt;
+  a.n_cnt = p.B * p.Hkv * tiles;
+  a.status = err;
+  return a;
+}
+
 // [tokens, heads, 128] bf16 tensor; box = 64 dims x box_h heads x box_t tokens.
 bool make_map(CUtensorMap* m, const void* base, int heads, long long tokens, int box_h, int box_t) {
   auto enc = encode_fn();
@@ -1152,11 +1174,11 @@ static int attn_tc_launch(const AttnParams& p, long long total_nodes, long long 
   // 64-key length buckets up to the longest possible last piece, a multiple of 32
   const int n_buckets = static_cast<int>(std::min<long long>(
       tc::kPlanBuckets, (std::min<long long>(p.piece_len, p.max_prefix) / 64 + 2 + 31) / 32 * 32));
-  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st, p.pre_off, p.B, p.piece_len,
-                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles,
-                      n_buckets, err);
+  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st,
+                      tc::plan_args(p, nq, tiles, n_buckets, err));
   if (rc != TV_OK) return rc;
-  return launch_pdl(tc::attn_tc_kernel<LIVE>, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
+  return launch_pdl(tc::attn_tc_kernel<LIVE>, dim3(p.Hkv, tiles, p.n_units / tiles), dim3(L::kThreads), L::kSmemBytes,
+                    st, P);
 }
 
 // 128-row tiles: attn_tc128_kernel (128-key blocks, two CTAs per SM)
@@ -1184,11 +1206,11 @@ static int attn_tc128_launch(const AttnParams& p, long long total_nodes, long lo
   const int tiles = (p.max_nodes + nq - 1) / nq;
   const int n_buckets = static_cast<int>(std::min<long long>(
       tc::kPlanBuckets, (std::min<long long>(p.piece_len, p.max_prefix) / 64 + 2 + 31) / 32 * 32));
-  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st, p.pre_off, p.B, p.piece_len,
-                      p.n_units / p.B, p.n_units, const_cast<int4*>(p.plan), p.piece_cnt, p.B * p.Hkv * tiles,
-                      n_buckets, err);
+  int rc = launch_pdl(tc::attn_plan_kernel, dim3(1), dim3(tc::kPlanThreads), 0, st,
+                      tc::plan_args(p, nq, tiles, n_buckets, err));
   if (rc != TV_OK) return rc;
-  return launch_pdl(tc::attn_tc128_kernel, dim3(p.Hkv, tiles, p.n_units), dim3(L::kThreads), L::kSmemBytes, st, P);
+  return launch_pdl(tc::attn_tc128_kernel, dim3(p.Hkv, tiles, p.n_units / tiles), dim3(L::kThreads), L::kSmemBytes,
+                    st, P);
 }
 
 int attn_tc(const AttnParams& p, long long total_nodes, long long total_prefix, int* err, cudaStream_t st) {
