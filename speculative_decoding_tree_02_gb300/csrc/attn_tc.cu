@@ -155,6 +155,23 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, int r, int n0,
 }
 
 // ------------------------------------------------------------------ kernel
+// Smallest node index set in a node's ancestor mask (1 << 30 when empty):
+// the mask words are read eight at a time, all loads of a batch in flight
+// together, instead of one dependent load per word.
+__device__ __forceinline__ int lowest_ancestor(const uint64_t* __restrict__ a, int words) {
+  for (int w0 = 0; w0 < words; w0 += 8) {
+    uint64_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = w0 + k < words ? a[w0 + k] : 0ull;
+    int lo = 1 << 30;
+#pragma unroll
+    for (int k = 7; k >= 0; --k)
+      if (v[k]) lo = (w0 + k) * 64 + __ffsll(static_cast<long long>(v[k])) - 1;
+    if (lo != 1 << 30) return lo;
+  }
+  return 1 << 30;
+}
+
 template <int LIVE>
 __global__ void __launch_bounds__(Lay<LIVE>::kThreads, 2) attn_tc_kernel(
     const __grid_constant__ TcParams P) {
@@ -199,10 +216,7 @@ __global__ void __launch_bounds__(Lay<LIVE>::kThreads, 2) attn_tc_kernel(
   if (active) {
     vis = p.vis_prefix ? p.vis_prefix[gn] : Pr;
     vis = min(max(vis, 0), Pr);
-    for (int w = 0; w < p.anc_words; ++w) {
-      const uint64_t a = p.anc[static_cast<int64_t>(gn) * p.anc_words + w];
-      if (a) { lowest = w * 64 + __ffsll(static_cast<long long>(a)) - 1; break; }
-    }
+    lowest = lowest_ancestor(p.anc + static_cast<int64_t>(gn) * p.anc_words, p.anc_words);
   }
   {
     const int vm = __reduce_max_sync(0xffffffffu, vis);
@@ -638,10 +652,7 @@ __global__ void __launch_bounds__(Lay2::kThreads, 1) attn_tc128_kernel(const __g
   if (active) {
     vis = p.vis_prefix ? p.vis_prefix[gn] : Pr;
     vis = min(max(vis, 0), Pr);
-    for (int w = 0; w < p.anc_words; ++w) {
-      const uint64_t a = p.anc[static_cast<int64_t>(gn) * p.anc_words + w];
-      if (a) { lowest = w * 64 + __ffsll(static_cast<long long>(a)) - 1; break; }
-    }
+    lowest = lowest_ancestor(p.anc + static_cast<int64_t>(gn) * p.anc_words, p.anc_words);
   }
   {
     const int vm = __reduce_max_sync(0xffffffffu, vis);
@@ -1008,34 +1019,36 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const PlanArgs 
   griddep_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) *a.status = 0;
-  for (int i = tid; i < a.n_cnt; i += kPlanThreads) a.piece_cnt[i] = 0;
   for (int i = tid; i < a.n_buckets; i += kPlanThreads) { s_hist[i] = 0; s_fill[i] = 0; }
-  __syncthreads();
   const int L = a.piece_len;
-  // pieces of tile t of request r and its visible keys; false: no nodes
-  auto tile_shape = [&](int r, int t, int& n, int& vk) {
+  const int pairs = a.B * a.tiles;   // <= n_cnt: the piece counters hold V_rt until the end
+  int* vk_of = a.piece_cnt;
+  // V_rt of every (request, tile), one warp per pair (-1: the tile has no nodes)
+  for (int e = warp; e < pairs; e += kPlanThreads / 32) {
+    const int r = e / a.tiles, t = e % a.tiles;
     const int n0 = a.node_off[r];
     const int N = a.node_off[r + 1] - n0;
     const int cnt = min(a.node_cnt ? min(a.node_cnt[r], N) : N, a.max_nodes);
     const int first = t * a.nq;
-    if (first >= cnt) return false;
     const int Pr = a.pre_off[r + 1] - a.pre_off[r];
-    vk = Pr;
+    int vk = Pr;
     if (a.vis_prefix) {
       vk = 0;
-      for (int i = first; i < min(first + a.nq, cnt); ++i) vk = max(vk, min(max(a.vis_prefix[n0 + i], 0), Pr));
+      for (int i = first + lane; i < min(first + a.nq, cnt); i += 32) vk = max(vk, min(max(a.vis_prefix[n0 + i], 0), Pr));
+      vk = __reduce_max_sync(0xffffffffu, vk);
     }
-    n = vk > 0 ? min((vk + L - 1) / L, a.max_pieces) : 1;
-    return true;
-  };
+    if (lane == 0) vk_of[e] = first < cnt ? vk : -1;
+  }
+  __syncthreads();
+  auto pieces = [&](int vk) { return vk > 0 ? min((vk + L - 1) / L, a.max_pieces) : 1; };
   auto bucket = [&](int vk, int n, int pc) {
     const int keys = pc < n - 1 ? L : vk - (n - 1) * L;
     return min(a.n_buckets - 1, (keys + 63) / 64);
   };
-  const int pairs = a.B * a.tiles;
   for (int e = tid; e < pairs; e += kPlanThreads) {
-    int n, vk;
-    if (!tile_shape(e / a.tiles, e % a.tiles, n, vk)) continue;
+    const int vk = vk_of[e];
+    if (vk < 0) continue;
+    const int n = pieces(vk);
     for (int pc = 0; pc < n; ++pc) atomicAdd(&s_hist[bucket(vk, n, pc)], 1);
   }
   __syncthreads();
@@ -1058,17 +1071,18 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const PlanArgs 
   }
   __syncthreads();
   for (int e = tid; e < pairs; e += kPlanThreads) {
-    const int r = e / a.tiles, t = e % a.tiles;
-    int n, vk;
-    if (!tile_shape(r, t, n, vk)) continue;
+    const int vk = vk_of[e];
+    if (vk < 0) continue;
+    const int n = pieces(vk);
     for (int pc = 0; pc < n; ++pc) {
       const int bk = bucket(vk, n, pc);
       const int pos = s_fill[bk] + atomicAdd(&s_hist[bk], -1) - 1;   // any slot of the bucket
-      a.plan[pos] = make_int4(r, pc, n, t);
+      a.plan[pos] = make_int4(e / a.tiles, pc, n, e % a.tiles);
     }
   }
-  __syncthreads();
   for (int u = s_total + tid; u < a.n_units; u += kPlanThreads) a.plan[u] = make_int4(-1, 0, 0, 0);   // no work
+  __syncthreads();
+  for (int i = tid; i < a.n_cnt; i += kPlanThreads) a.piece_cnt[i] = 0;
 }
 
 // ------------------------------------------------------------------ host side
