@@ -21,6 +21,8 @@
 // Then one thread per branch: running product of alpha in row order.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "tv_common.cuh"
 
 namespace tv {
@@ -396,8 +398,11 @@ __global__ void __cluster_dims__(kACluster, 1, 1) __launch_bounds__(kAClThreads,
 // Clusters that fit at once (a cluster sits in one GPC, so this can be below
 // the SM count times CTAs per SM over the cluster size).
 static int alpha_resident_clusters() {
-  static int cached = 0;
-  if (cached > 0) return cached;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];   // per device; 0: not measured yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (const int c = cache[dev].load(std::memory_order_relaxed)) return c;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kACluster);
   cfg.blockDim = dim3(kAClThreads);
@@ -405,11 +410,9 @@ static int alpha_resident_clusters() {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, alpha_cluster_kernel, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    int dev = 0, sms = 8;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    n = std::max(1, 2 * sms / kACluster);
+    n = std::max(1, 2 * sm_count() / kACluster);
   }
-  cached = n;
+  cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -8,13 +8,6 @@
 
 namespace {
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    return 148;
-  return n;
-}
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -44,14 +37,14 @@ WsLayout ws_layout(int B, int max_nodes, int max_prefix, int Hq, int Hkv, int d,
   w.status = 256;
   size_t parts = 0;   // partial rows
   if (w.tc) {
-    tv::attn_tc_shape(B, max_nodes, max_prefix, Hq, Hkv, sm_count(), &w.piece_len, &w.max_pieces, &w.tiles);
+    tv::attn_tc_shape(B, max_nodes, max_prefix, Hq, Hkv, tv::sm_count(), &w.piece_len, &w.max_pieces, &w.tiles);
     w.n_split = 1;
     w.n_units = B * w.tiles * w.max_pieces;   // (request, tile, piece) plan entries
     w.plan = align256(static_cast<size_t>(w.n_units) * sizeof(int4));
     w.cnt = align256(static_cast<size_t>(B) * Hkv * w.tiles * sizeof(int));
     if (w.max_pieces > 1) parts = static_cast<size_t>(w.max_pieces) * B * max_nodes * Hq;
   } else {
-    w.n_split = tv::attn_simt_splits(B, max_nodes, max_prefix, Hq, Hkv, sm_count());
+    w.n_split = tv::attn_simt_splits(B, max_nodes, max_prefix, Hq, Hkv, tv::sm_count());
     if (w.n_split > 1) parts = static_cast<size_t>(w.n_split) * B * max_nodes * Hq;
   }
   w.o_bytes = align256(parts * d * sizeof(float));

@@ -448,9 +448,7 @@ static bool mlp_tc_ok(int B, int V, int H, int64_t ld, const void* W1, const flo
 }
 
 int mlp_slices(int V, int H, int B) {
-  int dev = 0, n_sm = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int n_sm = sm_count();
   const int ctas_per_slice = (H / kMCols) * ((B + kMReq - 1) / kMReq);
   int s = (4 * n_sm + ctas_per_slice - 1) / ctas_per_slice;
   s = std::max(1, std::min(s, (V + kMSub - 1) / kMSub));
@@ -459,17 +457,12 @@ int mlp_slices(int V, int H, int B) {
 
 }  // namespace tv
 
-static int sm_count_mlp() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n;
-}
 
 TV_API size_t blockpilot_mlp_workspace_size(int B, int V, int H) {
   if (B <= 0 || V <= 0 || H <= 0) return 0;
   const size_t simt = static_cast<size_t>(tv::mlp_slices(V, H, B)) * B * H * sizeof(float);
   int ksteps = 0, kps = 0, splits = 0;
-  tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
+  tv::mlp_tc_shape(V, H, tv::sm_count(), &ksteps, &kps, &splits);
   const size_t Vp = (static_cast<size_t>(V) + 63) / 64 * 64;
   const size_t tcb = tv::kMlpHdrBytes + 16 * Vp * 2 + static_cast<size_t>(splits) * B * H * sizeof(float) +
                      tv::mlp_tail_bytes(B, H);
@@ -490,7 +483,7 @@ TV_API int blockpilot_mlp(const void* last_logits, int64_t ld, const float* row_
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (tv::mlp_tc_ok(B, V, H, ld, W1, b1)) {
     int ksteps = 0, kps = 0, splits = 0;
-    tv::mlp_tc_shape(V, H, sm_count_mlp(), &ksteps, &kps, &splits);
+    tv::mlp_tc_shape(V, H, tv::sm_count(), &ksteps, &kps, &splits);
     const int Vp = (V + 63) / 64 * 64;
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base);

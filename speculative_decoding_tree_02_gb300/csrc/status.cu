@@ -1,4 +1,5 @@
-// Status strings, version and per-device launch attributes of libtreeverify.
+// Status strings, version, per-device launch attributes and SM counts of libtreeverify.
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <tuple>
@@ -21,6 +22,20 @@ bool smem_limit(const void* kernel, int bytes) {
   }
   done.insert(key);
   return true;
+}
+
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];   // 0: not read yet
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < kMaxDevices && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace tv

@@ -24,6 +24,8 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 // device.  The attribute belongs to the device, so it is set once per
 // (kernel, device) and remembered; false when the runtime refuses.
 bool smem_limit(const void* kernel, int bytes);
+// Streaming multiprocessors of the current device (read once per device).
+int sm_count();
 template <typename... KArgs>
 inline bool smem_limit(void (*kernel)(KArgs...), int bytes) {
   return smem_limit(reinterpret_cast<const void*>(kernel), bytes);

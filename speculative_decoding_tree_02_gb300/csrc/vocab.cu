@@ -769,15 +769,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps) vocab_stream_merge_kernel(
                           row_lse, s_bv[wl], s_bi[wl]);
 }
 
-int sm_count_cached() {
-  static const int n = [] {
-    int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) return 148;
-    return c;
-  }();
-  return n;
-}
 
 // True for page-locked host memory the device reads in place.
 static bool host_resident(const void* p) {
@@ -807,8 +798,8 @@ int vocab_launch(const T* logits, int rows, int V, int64_t ld, const int32_t* ro
     // than HBM: a quarter of the SMs keep it busy and leave the rest to
     // kernels running beside this one.
     const int per_sm = sizeof(T) == 2 ? 4 : 2;   // shared memory: 3-slot rings of 16 KB / 32 KB chunks
-    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count_cached() / 4)
-                                                           : per_sm * sm_count_cached());
+    const int grid = std::min(items, host_resident(logits) ? std::max(1, sm_count() / 4)
+                                                           : per_sm * sm_count());
     auto* hdr = reinterpret_cast<StreamHdr*>(ws);
     auto* rec = reinterpret_cast<StreamRec*>(static_cast<uint8_t*>(ws) + kStreamHdrBytes);
     static const int planted = [] {
