@@ -95,61 +95,70 @@ struct TcParams {
 };
 
 // Merge of the pieces of one (request, KV head, tile), by the CTA of its last
-// piece to finish: all threads, two per query row (64 columns each), pieces
-// in order, so the result does not depend on which piece finished last.
+// piece to finish: thread item = (query row, 32 output columns), pieces in
+// order (weights 2^(m_i - M) l_i), so the result does not depend on which
+// piece finished last.  All loads of up to four pieces are issued before any
+// is used: one memory latency per item instead of one per piece.
 template <int LIVE>
 __device__ __forceinline__ void merge_pieces(const AttnParams& p, int r, int n0, int node_first, int cnt, int g,
                                              int kvh, int n_pieces, int nthreads) {
-  constexpr int kMaxP = 8;   // weights held in registers; more pieces recompute them
-  for (int rr = threadIdx.x >> 1; rr < LIVE; rr += nthreads / 2) {
+  constexpr int kGroup = 4;   // pieces whose loads are in flight together
+  for (int item = threadIdx.x; item < LIVE * 4; item += nthreads) {
+    const int rr = item >> 2, qd = item & 3;
     const int mln = node_first + rr / g;
     if (mln >= cnt) continue;
     const int mhead = kvh * g + rr % g;
-    const int half = threadIdx.x & 1;
     auto mslot = [&](int pc) {
       return (static_cast<int64_t>(pc) * p.B * p.max_nodes + static_cast<int64_t>(r) * p.max_nodes + mln) * p.Hq +
              mhead;
     };
-    float2 ml[kMaxP];
-#pragma unroll
-    for (int i = 0; i < kMaxP; ++i) ml[i] = i < n_pieces ? __ldcg(&p.ws_ml[mslot(i)]) : make_float2(-INFINITY, 0.f);
     float M = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kMaxP; ++i) M = fmaxf(M, ml[i].x);
-    for (int i = kMaxP; i < n_pieces; ++i) M = fmaxf(M, __ldcg(&p.ws_ml[mslot(i)].x));
+    if (n_pieces > kGroup)
+      for (int i = 0; i < n_pieces; ++i) M = fmaxf(M, __ldcg(&p.ws_ml[mslot(i)].x));
     float W = 0.f;
-    float acc[64];
+    float acc[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
-    auto add_piece = [&](float2 mi, int i) {
-      const float w = mi.y > 0.f ? ex2(mi.x - M) * mi.y : 0.f;   // empty piece: weight 0
-      W += w;
-      const float4* po = reinterpret_cast<const float4*>(p.ws_o + mslot(i) * kD + 64 * half);
-      float4 o4[16];
+    for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+    for (int i0 = 0; i0 < n_pieces; i0 += kGroup) {
+      float2 ml[kGroup];
+      float4 o4[kGroup][8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) o4[c] = __ldcg(po + c);
-      if (w == 0.f) return;   // (an empty piece's o was never written)
+      for (int k = 0; k < kGroup; ++k) {
+        ml[k] = make_float2(-INFINITY, 0.f);
+        if (i0 + k < n_pieces) {
+          ml[k] = __ldcg(&p.ws_ml[mslot(i0 + k)]);
+          const float4* po = reinterpret_cast<const float4*>(p.ws_o + mslot(i0 + k) * kD + 32 * qd);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        acc[4 * c] = fmaf(w, o4[c].x, acc[4 * c]);
-        acc[4 * c + 1] = fmaf(w, o4[c].y, acc[4 * c + 1]);
-        acc[4 * c + 2] = fmaf(w, o4[c].z, acc[4 * c + 2]);
-        acc[4 * c + 3] = fmaf(w, o4[c].w, acc[4 * c + 3]);
+          for (int c = 0; c < 8; ++c) o4[k][c] = __ldcg(po + c);
+        }
       }
-    };
+      if (n_pieces <= kGroup) {
 #pragma unroll
-    for (int i = 0; i < kMaxP; ++i)
-      if (i < n_pieces) add_piece(ml[i], i);
-    for (int i = kMaxP; i < n_pieces; ++i) add_piece(__ldcg(&p.ws_ml[mslot(i)]), i);
+        for (int k = 0; k < kGroup; ++k) M = fmaxf(M, ml[k].x);
+      }
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        const float w = ml[k].y > 0.f ? ex2(ml[k].x - M) * ml[k].y : 0.f;   // empty piece: weight 0
+        W += w;
+        if (w == 0.f) continue;   // (an empty piece's o was never written)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          acc[4 * c] = fmaf(w, o4[k][c].x, acc[4 * c]);
+          acc[4 * c + 1] = fmaf(w, o4[k][c].y, acc[4 * c + 1]);
+          acc[4 * c + 2] = fmaf(w, o4[k][c].z, acc[4 * c + 2]);
+          acc[4 * c + 3] = fmaf(w, o4[k][c].w, acc[4 * c + 3]);
+        }
+      }
+    }
     const float inv = W > 0.f ? 1.f / W : 0.f;
-    uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(n0 + mln) * p.Hq + mhead) * kD + 64 * half;
+    uint16_t* op = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(n0 + mln) * p.Hq + mhead) * kD + 32 * qd;
 #pragma unroll
-    for (int c = 0; c < 64; c += 8) {
+    for (int c = 0; c < 32; c += 8) {
       const uint4 v4 = make_uint4(pack_bf16(acc[c] * inv, acc[c + 1] * inv), pack_bf16(acc[c + 2] * inv, acc[c + 3] * inv),
                                   pack_bf16(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16(acc[c + 6] * inv, acc[c + 7] * inv));
       *reinterpret_cast<uint4*>(op + c) = v4;
     }
-    if (half == 0 && p.lse)
+    if (qd == 0 && p.lse)
       p.lse[static_cast<int64_t>(n0 + mln) * p.Hq + mhead] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
   }
 }
