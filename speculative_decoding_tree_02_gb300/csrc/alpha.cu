@@ -229,35 +229,72 @@ __device__ __forceinline__ float bmax8(uint4 x) {
                                            *reinterpret_cast<const __nv_bfloat162*>(&x.w)));
   return fmaxf(__low2float(h), __high2float(h));
 }
-// running (max, two partial sums) of exp over 8 bf16 logits
-__device__ __forceinline__ void online8(uint4 x, float& m, float& s0, float& s1) {
+// Packed fp32 pairs (sm_100 family): one FMA or add instruction computes two
+// values, each rounded as the scalar instruction would round it, so the two
+// passes issue about a fifth fewer instructions per element.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void upk2(uint64_t d, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the two bf16 of word w as an fp32 pair (low half first)
+__device__ __forceinline__ uint64_t bpair(uint32_t w) { return pk2(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ uint64_t ex2_pair(uint64_t a) {
+  float lo, hi;
+  upk2(a, lo, hi);
+  return pk2(ex2(lo), ex2(hi));
+}
+// running (max, pair of partial sums) of exp over 8 bf16 logits
+__device__ __forceinline__ void online8(uint4 x, float& m, uint64_t& s) {
   const float m8 = bmax8(x);
   if (m8 > m) {   // rescale (the sums are 0 while m is -inf)
     const float f = ex2((m - m8) * kLog2e);
-    s0 *= f;
-    s1 *= f;
+    float a, b;
+    upk2(s, a, b);
+    s = pk2(a * f, b * f);
     m = m8;
   }
   if (m != -INFINITY) {
     const float bm = m * kLog2e;
-    s0 += ex2(fmaf(bf16_lo(x.x), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.x), kLog2e, -bm));
-    s1 += ex2(fmaf(bf16_lo(x.y), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.y), kLog2e, -bm));
-    s0 += ex2(fmaf(bf16_lo(x.z), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.z), kLog2e, -bm));
-    s1 += ex2(fmaf(bf16_lo(x.w), kLog2e, -bm)) + ex2(fmaf(bf16_hi(x.w), kLog2e, -bm));
+    const uint64_t l2 = pk2(kLog2e, kLog2e), nb = pk2(-bm, -bm);
+    s = add2(s, ex2_pair(fma2(bpair(x.x), l2, nb)));
+    s = add2(s, ex2_pair(fma2(bpair(x.y), l2, nb)));
+    s = add2(s, ex2_pair(fma2(bpair(x.z), l2, nb)));
+    s = add2(s, ex2_pair(fma2(bpair(x.w), l2, nb)));
   }
+}
+__device__ __forceinline__ void online8(uint4 x, float& m, float& s0, float& s1) {
+  uint64_t s = pk2(s0, s1);
+  online8(x, m, s);
+  upk2(s, s0, s1);
 }
 // sum over 8 elements of 2^min(lp log2e - Lp, lq log2e - Lq)
 __device__ __forceinline__ void overlap8(uint4 x, uint4 y, float Lp, float Lq, float& a, float& b) {
-  a += ex2(fminf(fmaf(bf16_lo(x.x), kLog2e, -Lp), fmaf(bf16_lo(y.x), kLog2e, -Lq)));
-  b += ex2(fminf(fmaf(bf16_hi(x.x), kLog2e, -Lp), fmaf(bf16_hi(y.x), kLog2e, -Lq)));
-  a += ex2(fminf(fmaf(bf16_lo(x.y), kLog2e, -Lp), fmaf(bf16_lo(y.y), kLog2e, -Lq)));
-  b += ex2(fminf(fmaf(bf16_hi(x.y), kLog2e, -Lp), fmaf(bf16_hi(y.y), kLog2e, -Lq)));
-  a += ex2(fminf(fmaf(bf16_lo(x.z), kLog2e, -Lp), fmaf(bf16_lo(y.z), kLog2e, -Lq)));
-  b += ex2(fminf(fmaf(bf16_hi(x.z), kLog2e, -Lp), fmaf(bf16_hi(y.z), kLog2e, -Lq)));
-  a += ex2(fminf(fmaf(bf16_lo(x.w), kLog2e, -Lp), fmaf(bf16_lo(y.w), kLog2e, -Lq)));
-  b += ex2(fminf(fmaf(bf16_hi(x.w), kLog2e, -Lp), fmaf(bf16_hi(y.w), kLog2e, -Lq)));
+  const uint64_t l2 = pk2(kLog2e, kLog2e), np = pk2(-Lp, -Lp), nq = pk2(-Lq, -Lq);
+  uint64_t acc = pk2(a, b);
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float p0, p1, q0, q1;
+    upk2(fma2(bpair(xs[c]), l2, np), p0, p1);
+    upk2(fma2(bpair(ys[c]), l2, nq), q0, q1);
+    acc = add2(acc, pk2(ex2(fminf(p0, q0)), ex2(fminf(p1, q1))));
+  }
+  upk2(acc, a, b);
 }
-
 // Persistent clusters of 4 CTAs; cluster c takes rows c, c + NC, ...; CTA r
 // of a cluster owns elements [r S, (r + 1) S) of each row (S a multiple of 8).
 // Per row: pass 1 reads the slice from HBM (running max and sum of exp), one
