@@ -679,6 +679,44 @@ def test_vocab_status_word_clear_after_a_normal_call(tv):
 
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_attn_random_forests_bf16(tv, seed):
+    """Random request counts, tree sizes (one node to a few 128-row tiles),
+    prefix lengths (zero to a few thousand keys), per-node visible prefixes or
+    none, and node_cnt or none: whatever tile size, piece count and plan order
+    the call takes, every verified output matches the oracle."""
+    rng = synth.make_rng(63, seed)
+    B = int(rng.integers(1, 6))
+    sizes = [int(x) for x in rng.integers(1, 150, B)]
+    parent = np.concatenate([synth.random_tree(rng, n, int(rng.integers(1, 12))) for n in sizes])
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    plen = rng.integers(0, 3000, B).astype(np.int32)
+    vis = None
+    if seed % 2:
+        vis = np.concatenate([rng.integers(0, plen[r] + 1, sizes[r]) for r in range(B)]).astype(np.int32)
+    cnt = np.array([int(rng.integers(1, n + 1)) for n in sizes], np.int32) if seed % 3 == 0 else None
+    att = synth.attention_tensors(rng, int(off[-1]), max(1, int(plen.sum())), 32, 8, 128, "bf16")
+    d = dict(parent=parent, node_off=off, pre_off=np.concatenate([[0], np.cumsum(plen)]).astype(np.int32),
+             vis_prefix=vis, dtype="bf16", **att)
+    run_attn(tv, d, node_cnt=cnt)
+
+
+@pytest.mark.parametrize("sizes,cnt,P", [([70, 45, 130], [50, 45, 7], 900), ([160, 33], [129, 1], 2500)])
+def test_attn_128_row_tiles_node_cnt_and_visible_prefixes(tv, sizes, cnt, P):
+    """128-row tiles whose requests are cut short by node_cnt (only the first
+    cnt nodes verified) and whose nodes see per-node prefixes: the planner's
+    per-tile visible keys and node counts decide the pieces and their order."""
+    rng = synth.make_rng(62, len(sizes) * 1000 + P)
+    parent = np.concatenate([synth.random_tree(rng, n, 9) for n in sizes])
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    plen = rng.integers(P // 3, P + 1, len(sizes)).astype(np.int32)
+    vis = np.concatenate([rng.integers(0, plen[r] + 1, sizes[r]) for r in range(len(sizes))]).astype(np.int32)
+    att = synth.attention_tensors(rng, int(off[-1]), int(plen.sum()), 32, 8, 128, "bf16")
+    d = dict(parent=parent, node_off=off, pre_off=np.concatenate([[0], np.cumsum(plen)]).astype(np.int32),
+             vis_prefix=vis, dtype="bf16", **att)
+    run_attn(tv, d, node_cnt=np.array(cnt, np.int32))
+
+
 @pytest.mark.parametrize("sizes,P", [([80, 40, 1, 33], 700), ([96], 3000), ([200, 130], 257)])
 def test_attn_128_row_tiles_ragged(tv, sizes, P):
     """128-row tiles with 128-key blocks: several tiles per request, ragged
