@@ -437,6 +437,27 @@ __global__ void stream_hdr_clear_kernel(StreamHdr* hdr, int status0) {
   hdr->claim = 0;
 }
 
+// Largest bf16 of this lane's share of a 1024-element segment (16-byte
+// words lane-interleaved; words at or past V count as -inf), compared as
+// packed bf16 pairs.
+__device__ __forceinline__ float seg_max_bf16(const uint8_t* p, int e_first, int V) {
+  constexpr int NV = kSegLen / 8 / 32;   // 16-byte words per lane
+  const int lane = threadIdx.x & 31;
+  const uint32_t ninf = 0xff80ff80u;     // (-inf, -inf)
+  __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&ninf);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int e0 = e_first + (j * 32 + lane) * 8;
+    uint4 w = make_uint4(ninf, ninf, ninf, ninf);
+    if (e0 < V) w = *reinterpret_cast<const uint4*>(p + static_cast<size_t>((j * 32 + lane) * 16));
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&w.w));
+    m = __hmax2(m, __hmax2(a, b));
+  }
+  return fmaxf(__low2float(m), __high2float(m));
+}
 // Elements of segment `seg` of a row visible to this lane: 4 (bf16) or 8
 // (fp32) 16-byte vectors, lane-interleaved; entries at or past V become -inf.
 template <typename T>
@@ -717,22 +738,30 @@ __global__ void __launch_bounds__(kStreamThreads, 4) vocab_stream_kernel(
     if (item < 0) return;
     const int c = s_chunk[s];
     const int e_first = c * kVChunk + warp * kSegLen;
-    float v[EPT];
-    seg_values<T>(ring + s * kSChunkBytes + static_cast<size_t>(warp) * kSegLen * sizeof(T), e_first, V, v);
-    __syncwarp();
-    if (lane == 0) bar_arrive_plain(sm_u32(&empty[s]));   // this warp is done with the slot
-    float m4[4] = {v[0], v[1], v[2], v[3]};
+    const uint8_t* seg = ring + s * kSChunkBytes + static_cast<size_t>(warp) * kSegLen * sizeof(T);
+    float wmax, wsum = 0.f;
+    if constexpr (sizeof(T) == 2 && !LSE) {
+      // maximum only: packed bf16 pairs straight from the ring, no unpacking
+      wmax = redux_max(seg_max_bf16(seg, e_first, V));
+      __syncwarp();
+      if (lane == 0) bar_arrive_plain(sm_u32(&empty[s]));   // this warp is done with the slot
+    } else {
+      float v[EPT];
+      seg_values<T>(seg, e_first, V, v);
+      __syncwarp();
+      if (lane == 0) bar_arrive_plain(sm_u32(&empty[s]));   // this warp is done with the slot
+      float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-    for (int t = 4; t < EPT; ++t) m4[t & 3] = fmaxf(m4[t & 3], v[t]);
-    const float wmax = redux_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-    float wsum = 0.f;
-    if constexpr (LSE) {
-      if (wmax != -INFINITY) {
-        const float mb = wmax * kLog2e;
+      for (int t = 4; t < EPT; ++t) m4[t & 3] = fmaxf(m4[t & 3], v[t]);
+      wmax = redux_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      if constexpr (LSE) {
+        if (wmax != -INFINITY) {
+          const float mb = wmax * kLog2e;
 #pragma unroll
-        for (int t = 0; t < EPT; ++t) wsum += ex2(fmaf(v[t], kLog2e, -mb));
+          for (int t = 0; t < EPT; ++t) wsum += ex2(fmaf(v[t], kLog2e, -mb));
+        }
+        wsum = warp_sum(wsum);
       }
-      wsum = warp_sum(wsum);
     }
     if (lane == 0) {
       StreamRec* r = rec + item;
