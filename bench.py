@@ -265,7 +265,10 @@ def make_step(tv, torch, hd, rho, logits=None):
     # rows, and the acceptance / table update / retrieval chain needs only the
     # vocabulary results.  So attention runs on a second stream, forked after
     # the launch of dcut_select and joined at the end of the step, while the
-    # vocabulary chain runs on the caller's stream.
+    # vocabulary chain runs on the caller's stream.  The vocabulary pass is
+    # captured before the attention launch so that its stream kernel takes
+    # the SMs first and the attention CTAs fill them as it drains (the other
+    # order measured 0.3-0.6 us slower).
     side = torch.cuda.Stream(priority=-1)
     ev_fork, ev_sel, ev_join = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
 
@@ -277,11 +280,11 @@ def make_step(tv, torch, hd, rho, logits=None):
             k_prep()
         k_dcut()
         ev_sel.record(cur)
+        k_vocab()
         with torch.cuda.stream(side):
             side.wait_event(ev_sel)
             k_attn()
             ev_join.record(side)
-        k_vocab()
         k_accept()
         k_adj()
         k_retr()
