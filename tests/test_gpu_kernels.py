@@ -717,11 +717,12 @@ def test_attn_128_row_tiles_node_cnt_and_visible_prefixes(tv, sizes, cnt, P):
     run_attn(tv, d, node_cnt=np.array(cnt, np.int32))
 
 
-@pytest.mark.parametrize("sizes,P", [([80, 40, 1, 33], 700), ([96], 3000), ([200, 130], 257)])
+@pytest.mark.parametrize("sizes,P", [([80, 40, 1, 33], 700), ([96], 3000), ([200, 130], 257), ([61], 8192),
+                                     ([29], 5000)])
 def test_attn_128_row_tiles_ragged(tv, sizes, P):
     """128-row tiles with 128-key blocks: several tiles per request, ragged
     last tiles, a one-node request, and key pieces with their merge (few
-    tiles over a long prefix)."""
+    tiles over a long prefix: up to four 2048-key pieces, a ragged last one)."""
     rng = synth.make_rng(61, len(sizes) * 1000 + P)
     parent = np.concatenate([synth.random_tree(rng, n, 9) for n in sizes])
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
